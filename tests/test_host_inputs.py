@@ -1,0 +1,47 @@
+"""Host-side logic: chunk partition (hybrid alpha family) and workload recipe."""
+import numpy as np
+
+from chunked_linear_recurrence_gated_gb300.inputs import (cu_seqlens, make_inputs,
+                                                          varlen_lengths, workloads)
+from chunked_linear_recurrence_gated_gb300.partition import hybrid_boundaries
+
+
+def test_hybrid_partition_alpha_half():
+    # a = L_lin C_lin + C_dense = 4, b = 1: f(x) = 4x + x^2/2; boundaries blend
+    # i*T/N with the equal-cost offsets, rounded half-up to 64.
+    b = hybrid_boundaries(131072, 8, 0.5)
+    assert b == [0, 31360, 49152, 64704, 79104, 92800, 105920, 118656, 131072]
+
+
+def test_hybrid_partition_limits():
+    T, N = 65536, 4
+    assert hybrid_boundaries(T, N, 0.0) == [0, 16384, 32768, 49152, 65536]
+    b1 = hybrid_boundaries(T, N, 1.0)
+    f = lambda x: 4 * x + x * x / 2
+    costs = [f(b1[i + 1]) - f(b1[i]) for i in range(N)]
+    assert max(costs) / min(costs) < 1.01  # equal cost up to 64-rounding
+    assert all(x % 64 == 0 for x in b1)
+
+
+def test_varlen_lengths_recipe():
+    L = varlen_lengths()
+    assert sum(L) == 131072
+    assert all(x % 64 == 0 and 64 <= x <= 65536 for x in L)
+    cu = cu_seqlens(L).numpy()
+    assert cu[0] == 0 and cu[-1] == 131072 and np.all(np.diff(cu) > 0)
+
+
+def test_workloads_shapes():
+    ws = workloads()
+    assert [sum(w.chunks) for w in ws[:4]] == [w.T for w in ws[:4]]
+    assert all(c % 64 == 0 for w in ws[:4] for c in w.chunks)
+
+
+def test_inputs_seeded_and_normalised():
+    a = make_inputs(1, 70, 2, 16, 8, seed=5)
+    b = make_inputs(1, 70, 2, 16, 8, seed=5)
+    for key in a:
+        assert a[key].equal(b[key])
+    n = a["k"].float().norm(dim=-1)
+    assert (n - 1).abs().max() < 1e-2
+    assert (a["g"].float() < 0).all() and ((a["beta"].float() > 0) & (a["beta"].float() < 1)).all()
