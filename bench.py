@@ -1,0 +1,406 @@
+"""Benchmark: chunk-level Gated DeltaNet fwd+bwd tokens/s on one GB300.
+
+Workload: B=1, H=16, d_k=d_v=128, T=262144 bf16 (fp32 state), split into 8
+chunks of 32768 run in order through gdn_chunk_fwd (state chained forward),
+then in reverse through gdn_chunk_bwd (state gradient chained backward),
+do ~ N(0,1)*0.02, dS_out = 0 at the sequence end. One step = that whole
+forward + backward pass. Inputs are synthetic (seeded) and larger than L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun) every rank runs its own independent sequence (weak
+scaling; heads and sequences share nothing, so there is no collective) and
+`value` is the total tokens of all ranks per second. Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "GDN chunk fwd+bwd tokens/s at H=16,d=128,256K on 1 GB300; % of roofline"
+UNIT = "tokens/s"
+WORKLOAD_INDEX = 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- algorithmic model
+def alg_bytes_per_token_head(dk, dv, esz=2):
+    """Bytes the method must move per token-head: fwd reads q,k,v (+g,beta) and
+    writes o; bwd reads q,k,v,g,beta,do and writes dq,dk,dv,dg,dbeta."""
+    fwd = esz * (2 * dk + dv) + 2 * esz + esz * dv
+    bwd = esz * (2 * dk + dv + dv) + 2 * esz + esz * (2 * dk + dv) + 2 * esz
+    return fwd, bwd
+
+
+def alg_flops_per_token_head(dk, dv, C=64):
+    fwd = 2 * C * (3 * dk + 2 * dv) + 6 * dk * dv + C * C / 3
+    bwd = 18 * C * dk + 10 * C * dv + 16 * dk * dv + 4 * C * C + C * C / 3
+    return fwd, bwd
+
+
+# Per-kernel algorithmic work per 64-token block-head (C = 64), used for the
+# dominant kernel's roofline: bytes the kernel must move in this design
+# (inputs, outputs and workspace intermediates it reads or writes), and the
+# contraction flops it must do.
+def kernel_model(name, dk, dv, esz=2, C=64):
+    f4 = 4
+    if name == "simt_pre":
+        by = C * (dk + dv) * esz + 2 * C * esz + C * (dk + dv) * f4 + C * f4
+        fl = 2 * C * C * dk + C ** 3 / 3 + 2 * C * C * dk + 2 * C * C * dv
+    elif name == "simt_st":
+        by = C * (dk + dv) * f4 + C * dk * esz + C * f4 + dk * dv * f4 + C * dv * f4
+        fl = 4 * C * dk * dv
+    elif name == "simt_out":
+        by = 2 * C * dk * esz + C * f4 + dk * dv * f4 + C * dv * f4 + C * dv * esz
+        fl = 2 * C * dk * dv + 2 * C * C * dk + 2 * C * C * dv
+    elif name == "simt_st_bwd":
+        by = 2 * C * dk * esz + C * dk * f4 + C * dv * esz + C * f4 + dk * dv * f4 + C * dv * f4
+        fl = 2 * C * C * dk + 2 * C * C * dv + 6 * C * dk * dv
+    elif name == "simt_grad":
+        by = (C * (2 * dk + 2 * dv) * esz + 2 * C * esz + 2 * dk * dv * f4 + 2 * C * dv * f4
+              + C * C * f4 + C * f4 + C * (2 * dk + dv) * esz + 2 * C * esz)
+        fl = 6 * C * dk * dv + 10 * C * C * dk + 6 * C * C * dv + 4 * C ** 3
+    else:
+        return None
+    return by, fl
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+        return False
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the step
+class Runner:
+    def __init__(self, w, dev, seed_offset=0):
+        from chunked_linear_recurrence_gated_gb300 import gdn
+        from chunked_linear_recurrence_gated_gb300.inputs import make_workload_inputs
+
+        self.gdn = gdn
+        self.w = w
+        self.dev = dev
+        x = make_workload_inputs(w, device=dev)
+        self.x = x
+        B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+        self.o = torch.empty(B, T, H, dv, dtype=w.torch_dtype, device=dev)
+        self.dq = torch.empty_like(x["q"])
+        self.dk = torch.empty_like(x["k"])
+        self.dv = torch.empty_like(x["v"])
+        self.dg = torch.empty_like(x["g"])
+        self.db = torch.empty_like(x["beta"])
+        n = len(w.chunks)
+        self.S = [torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev) for _ in range(n + 1)]
+        self.S[0].zero_()
+        self.dS = [torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev) for _ in range(n)]
+        self.bounds = np.concatenate([[0], np.cumsum(w.chunks)]).astype(int)
+        Lmax = max(w.chunks)
+        shp = gdn.gdn_shape(B, Lmax, H, dk, dv, 1 if w.dtype == "bf16" else 0)
+        self.ws_f = gdn.alloc_workspace(gdn.chunk_workspace_bytes(shp, False), dev)
+        self.ws_b = gdn.alloc_workspace(gdn.chunk_workspace_bytes(shp, True), dev)
+        self.launches_per_step = None
+
+    def sl(self, t, i):
+        return t[:, self.bounds[i]:self.bounds[i + 1]]
+
+    def step(self):
+        g, x = self.gdn, self.x
+        n = len(self.w.chunks)
+        for i in range(n):
+            g.gdn_chunk_fwd(self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
+                            self.sl(x["g"], i), self.sl(x["beta"], i), S_in=self.S[i],
+                            o=self.sl(self.o, i), S_out=self.S[i + 1], workspace=self.ws_f)
+        for i in reversed(range(n)):
+            g.gdn_chunk_bwd(self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
+                            self.sl(x["g"], i), self.sl(x["beta"], i), self.S[i],
+                            self.sl(x["do"], i), dS_out=self.dS[i + 1] if i + 1 < n else None,
+                            grads=(self.sl(self.dq, i), self.sl(self.dk, i), self.sl(self.dv, i),
+                                   self.sl(self.dg, i), self.sl(self.db, i)),
+                            dS_in=self.dS[i], workspace=self.ws_b)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def time_steps(fn, K, dev):
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    s.record()
+    for _ in range(K):
+        fn()
+    e.record()
+    torch.cuda.synchronize(dev)
+    return s.elapsed_time(e)
+
+
+def e2e_measure(runner, K, dev):
+    """Same step through the public API with host buffers: pinned host inputs
+    copied in and results (o and every gradient) copied out inside the timed region."""
+    x = runner.x
+    keys = ["q", "k", "v", "g", "beta", "do"]
+    host_in = {k: torch.empty(x[k].shape, dtype=x[k].dtype, pin_memory=True) for k in keys}
+    for k in keys:
+        host_in[k].copy_(x[k])
+    outs = [runner.o, runner.dq, runner.dk, runner.dv, runner.dg, runner.db]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        for k in keys:
+            x[k].copy_(host_in[k], non_blocking=True)
+        runner.step()
+        for h, t in zip(host_out, outs):
+            h.copy_(t, non_blocking=True)
+
+    one()
+    ms = time_steps(one, K, dev)
+    return ms / K, h2d, d2h
+
+
+def cpu_baseline(w, x, max_tokens=32768):
+    """The oracle, as it stands, on a bounded sample: all heads of the first chunk."""
+    import oracle
+
+    L = min(max_tokens, w.chunks[0])
+    sub = {k: x[k][:, :L].float().cpu() for k in ("q", "k", "v", "g", "beta", "do")}
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.fwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], None, nthreads=threads)
+    oracle.bwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], None, sub["do"], None,
+               nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": L / dt, "unit": UNIT, "cores": min(threads, w.H * w.B), "kind": "oracle",
+            "sample": f"fwd+bwd of the first {L} tokens of the sequence, all {w.H} heads "
+                      f"(fp64 token loop, {dt:.1f} s)"}
+
+
+def reference_arm(args, w):
+    """The oracle timed on the host cores, a bounded sample per step."""
+    import oracle
+    from chunked_linear_recurrence_gated_gb300.inputs import make_workload_inputs
+
+    x = make_workload_inputs(w, device="cpu")
+    L = 2048
+    sub = {k: x[k][:, :L].float() for k in ("q", "k", "v", "g", "beta", "do")}
+    threads = oracle.default_threads()
+
+    def one():
+        oracle.fwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], None, nthreads=threads)
+        oracle.bwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], None, sub["do"], None,
+                   nthreads=threads)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = L / dt
+    sample = f"fwd+bwd of the first {L} tokens, all {w.H} heads, per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample_tokens": L},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(threads, w.H),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    from chunked_linear_recurrence_gated_gb300.inputs import workload
+
+    w = workload(WORKLOAD_INDEX)
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args, w)))
+        return
+
+    from chunked_linear_recurrence_gated_gb300 import gdn
+
+    gdn.load()  # fails loudly if the CUDA library is missing
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+
+    runner = Runner(w, dev)
+    for _ in range(max(args.warmup, 3)):
+        runner.step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        ms = time_steps(runner.step, args.steps, dev)
+    barrier(world)
+    ms_step = ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tokens = w.B * w.T * world
+    value = tokens / (ms_step / 1e3)
+
+    # per-kernel timing on the launch stream (instrumented replay of the same steps)
+    timer = gdn.KernelTimer(capacity=4096)
+    with timer:
+        for _ in range(min(2, args.steps)):
+            runner.step()
+    torch.cuda.synchronize(dev)
+    per = timer.per_kernel()
+    nsteps_timed = min(2, args.steps)
+    launches = sum(len(v) for v in per.values()) // nsteps_timed
+    totals = {k: sum(v) for k, v in per.items()}
+    dom = max(totals, key=totals.get)
+    avg_ms = totals[dom] / len(per[dom])
+    hbm, bf16, bf16_s, peak_kind = peaks()
+    nblk_heads = (max(w.chunks) // 64) * w.H  # block-heads in one launch of a chunk kernel
+    km = kernel_model(dom, w.dk, w.dv)
+    if km is not None:
+        by, fl = km
+        if dom.startswith("simt_"):
+            # fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock (2070 MHz)
+            alu_peak = 152 * 128 * 2 * 2.070e9 / 1e12
+            achieved = fl * nblk_heads / (avg_ms / 1e3) / 1e12
+            roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                    "frac": achieved / alu_peak, "traffic": None, "kernel": dom,
+                    "peak_source": "derived: fp32 FFMA lanes x max clock"}
+        else:
+            achieved = by * nblk_heads / (avg_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved / hbm, "traffic": None, "kernel": dom,
+                    "peak_source": peak_kind}
+    else:
+        roof = {"bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
+                "traffic": None, "kernel": dom}
+    fb, bb = alg_bytes_per_token_head(w.dk, w.dv)
+    ff, bf = alg_flops_per_token_head(w.dk, w.dv)
+    th = w.B * w.T * w.H
+    t_bytes = (fb + bb) * th / (hbm * 1e9)
+    t_flops = (ff + bf) * th / (bf16 * 1e12)
+    roof_ms = max(t_bytes, t_flops) * 1e3
+    op_roofline = {"roofline_ms": roof_ms, "bound": "hbm" if t_bytes >= t_flops else "tensor",
+                   "frac_of_roofline": roof_ms / ms_step,
+                   "roofline_tokens_per_s": w.B * w.T / (roof_ms / 1e3)}
+
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = e2e_measure(runner, max(1, min(args.steps, 3)), dev)
+        e2e = {"value": tokens / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, runner.x)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk,
+                       "dv": w.dv, "chunks": w.chunks, "state": "fp32",
+                       "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"dp{world} (independent sequence per GPU)"},
+            "clocks": clk.summary(),
+            "e2e": e2e,
+            "gpu_launches": launches * args.steps,
+            "roofline": roof,
+            "op_roofline": op_roofline,
+            "kernels_ms_per_step": {k: v / nsteps_timed for k, v in totals.items()},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

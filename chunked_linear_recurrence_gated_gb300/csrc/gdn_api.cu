@@ -1,0 +1,361 @@
+// C-ABI entry points (include/gdn.h): argument checks, workspace carving,
+// varlen block tables, and dispatch to the kernel families.
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+#include "../../include/gdn_profile.h"
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+// ------------------------------------------------------------ timing hook
+namespace {
+cudaEvent_t* g_prof_ev = nullptr;
+int g_prof_cap = 0;
+int g_prof_n = 0;
+const char* g_prof_names[4096];
+}  // namespace
+
+void prof_mark(cudaStream_t st, const char* next) {
+  if (!g_prof_ev || g_prof_n >= g_prof_cap) return;
+  if (cudaEventRecord(g_prof_ev[g_prof_n], st) != cudaSuccess) return;
+  g_prof_names[g_prof_n] = next;
+  ++g_prof_n;
+}
+
+// ------------------------------------------------------------ varlen block tables
+// One CTA: validates cu_seqlens (cu[0] = 0, non-decreasing, cu[nseq] = T),
+// numbers the 64-token blocks of every sequence (each sequence's grid starts
+// at its first token) and records the owning sequence of each block. A
+// malformed array sets the status word and leaves every table empty, so no
+// kernel does any work.
+__global__ void k_varlen_prep(const int* __restrict__ cu, int nseq, int T, int nblk_cap,
+                              int* blk0, int* blk_seq, int* status) {
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = (cu[0] != 0 || cu[nseq] != T) ? 1 : 0;
+  __syncthreads();
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x)
+    if (cu[s + 1] < cu[s]) bad = 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int s = 0; s < nseq; ++s) {
+      blk0[s] = acc;
+      if (!bad) acc += (cu[s + 1] - cu[s] + BT - 1) / BT;
+    }
+    blk0[nseq] = acc;
+    if (acc > nblk_cap) bad = 1;  // cannot happen for a valid array
+    status[0] = bad ? DEV_BAD_CU_SEQLENS : DEV_OK;
+  }
+  __syncthreads();
+  if (bad) {
+    for (int gb = threadIdx.x; gb < nblk_cap; gb += blockDim.x) blk_seq[gb] = -1;
+    for (int s = threadIdx.x; s <= nseq; s += blockDim.x) blk0[s] = 0;
+    return;
+  }
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x)
+    for (int gb = blk0[s]; gb < blk0[s + 1]; ++gb) blk_seq[gb] = s;
+  for (int gb = blk0[nseq] + threadIdx.x; gb < nblk_cap; gb += blockDim.x) blk_seq[gb] = -1;
+}
+
+cudaError_t varlen_prep(const int* cu, int nseq, int T, int nblk_cap, int* blk0, int* blk_seq,
+                        int* status, cudaStream_t st) {
+  prof_mark(st, "varlen_prep");
+  k_varlen_prep<<<1, 1024, 0, st>>>(cu, nseq, T, nblk_cap, blk0, blk_seq, status);
+  return cudaGetLastError();
+}
+
+__global__ void k_status_ok(int* status) { status[0] = DEV_OK; }
+
+}  // namespace gdn
+
+namespace {
+
+using namespace gdn;
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+struct Plan {
+  int B, T, H, dk, dv, dtype;
+  int nseq;       // sequences (B for fixed-length calls)
+  int nblk_cap;   // global 64-token blocks launched
+  bool varlen;
+};
+
+bool supported(const gdn_shape* s) {
+  return (s->dtype == GDN_DTYPE_F32 || s->dtype == GDN_DTYPE_BF16) &&
+         (s->dk == 64 || s->dk == 128) && (s->dv == 64 || s->dv == 128 || s->dv == 256);
+}
+
+gdn_status plan_shape(const gdn_shape* s, bool varlen, int nseq, Plan* p) {
+  if (!s) return GDN_ERR_INVALID_ARG;
+  if (s->B < 1 || s->T < 0 || s->H < 1 || s->H > 65535 || s->dk < 1 || s->dv < 1)
+    return GDN_ERR_INVALID_ARG;
+  if (!supported(s)) return GDN_ERR_UNSUPPORTED;
+  p->B = s->B; p->T = s->T; p->H = s->H; p->dk = s->dk; p->dv = s->dv; p->dtype = s->dtype;
+  p->varlen = varlen;
+  const long long nbs = ((long long)s->T + BT - 1) / BT;
+  long long nblk;
+  if (varlen) {
+    if (s->B != 1 || nseq < 1) return GDN_ERR_INVALID_ARG;
+    p->nseq = nseq;
+    nblk = nbs + nseq;
+  } else {
+    p->nseq = s->B;
+    nblk = nbs * s->B;
+  }
+  if (nblk > (1ll << 30) || (long long)p->nseq * p->H * (p->dv / 16) > (1ll << 30) ||
+      (long long)s->B * s->T > (1ll << 31) - 1)
+    return GDN_ERR_INVALID_ARG;
+  p->nblk_cap = (int)nblk;
+  return GDN_OK;
+}
+
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off = up(off + bytes);
+    return o;
+  }
+};
+
+// Workspace layout of the SIMT kernels. The first 256 bytes hold the status word.
+size_t simt_layout(const Plan& p, bool bwd, SimtWs* ws, int** blk0, int** blk_seq, char* base) {
+  Carve c;
+  const size_t nbh = (size_t)p.nblk_cap * p.H;
+  const size_t o_status = c.take(kAlign);
+  const size_t o_blk0 = p.varlen ? c.take(sizeof(int) * (p.nseq + 1)) : 0;
+  const size_t o_blks = p.varlen ? c.take(sizeof(int) * (size_t)p.nblk_cap) : 0;
+  const size_t o_gam = c.take(4 * nbh * BT);
+  const size_t o_W = c.take(4 * nbh * BT * p.dk);
+  const size_t o_U = c.take(4 * nbh * BT * p.dv);
+  const size_t o_Hb = c.take(4 * nbh * p.dk * p.dv);
+  const size_t o_Vn = c.take(4 * nbh * BT * p.dv);
+  size_t o_T = 0, o_dH = 0, o_dVn = 0;
+  if (bwd) {
+    o_T = c.take(4 * nbh * BT * BT);
+    o_dH = c.take(4 * nbh * p.dk * p.dv);
+    o_dVn = c.take(4 * nbh * BT * p.dv);
+  }
+  if (base) {
+    ws->status = (int*)(base + o_status);
+    ws->gam = (float*)(base + o_gam);
+    ws->W = (float*)(base + o_W);
+    ws->U = (float*)(base + o_U);
+    ws->Hb = (float*)(base + o_Hb);
+    ws->Vn = (float*)(base + o_Vn);
+    ws->Tm = bwd ? (float*)(base + o_T) : nullptr;
+    ws->dH = bwd ? (float*)(base + o_dH) : nullptr;
+    ws->dVn = bwd ? (float*)(base + o_dVn) : nullptr;
+    *blk0 = p.varlen ? (int*)(base + o_blk0) : nullptr;
+    *blk_seq = p.varlen ? (int*)(base + o_blks) : nullptr;
+  }
+  return c.off;
+}
+
+size_t ws_bytes(const Plan& p, bool bwd) {
+  SimtWs w;
+  int *a, *b;
+  return simt_layout(p, bwd, &w, &a, &b, nullptr);
+}
+
+bool al(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+// Tensor arguments: [.., d] tensors need 16-byte alignment, [B, T, H] tensors
+// element alignment; states 16 bytes. Returns false on a violation.
+bool check_tensor(const void* p, bool required, size_t align) {
+  if (!p) return !required;
+  return al(p, align);
+}
+
+SeqMap make_map(const Plan& p, const int* cu, const int* blk0, const int* blk_seq) {
+  SeqMap m;
+  m.cu = p.varlen ? cu : nullptr;
+  m.blk0 = blk0;
+  m.blk_seq = blk_seq;
+  m.nseq = p.nseq;
+  m.T_fixed = p.varlen ? 0 : p.T;
+  m.nblk_fixed = p.varlen ? 0 : (p.T + BT - 1) / BT;
+  m.nblk_cap = p.nblk_cap;
+  m.H = p.H;
+  return m;
+}
+
+gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const float* S_in, void* o, float* S_out,
+                   void* ws, size_t wsb, void* stream) {
+  const size_t esz = p.dtype == GDN_DTYPE_F32 ? 4 : 2;
+  const bool any = p.T > 0;
+  if (!check_tensor(q, any, 16) || !check_tensor(k, any, 16) || !check_tensor(v, any, 16) ||
+      !check_tensor(g, any, esz) || !check_tensor(beta, any, esz) || !check_tensor(o, any, 16) ||
+      !check_tensor(S_in, false, 16) || !check_tensor(S_out, false, 16))
+    return GDN_ERR_INVALID_ARG;
+  if (p.varlen && (!cu || !al(cu, 4))) return GDN_ERR_INVALID_ARG;
+  if (!ws || !al(ws, kAlign) || wsb < ws_bytes(p, false)) return GDN_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  SimtWs w;
+  int *blk0, *blk_seq;
+  simt_layout(p, false, &w, &blk0, &blk_seq, (char*)ws);
+  cudaError_t e;
+  if (p.varlen)
+    e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st);
+  else {
+    prof_mark(st, "status");
+    k_status_ok<<<1, 1, 0, st>>>(w.status);
+    e = cudaGetLastError();
+  }
+  if (e) return GDN_ERR_CUDA;
+  const SeqMap m = make_map(p, cu, blk0, blk_seq);
+  e = simt_fwd(m, p.dk, p.dv, p.dtype, q, k, v, g, beta, S_in, o, S_out, w, st);
+  return e ? GDN_ERR_CUDA : GDN_OK;
+}
+
+gdn_status run_bwd(const Plan& p, const int* cu, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const float* S_in, const void* dout,
+                   const float* dS_out, void* dq, void* dk, void* dv, void* dg, void* dbeta,
+                   float* dS_in, void* ws, size_t wsb, void* stream) {
+  const size_t esz = p.dtype == GDN_DTYPE_F32 ? 4 : 2;
+  const bool any = p.T > 0;
+  if (!check_tensor(q, any, 16) || !check_tensor(k, any, 16) || !check_tensor(v, any, 16) ||
+      !check_tensor(g, any, esz) || !check_tensor(beta, any, esz) ||
+      !check_tensor(dout, any, 16) || !check_tensor(dq, any, 16) ||
+      !check_tensor(dk, any, 16) || !check_tensor(dv, any, 16) || !check_tensor(dg, any, esz) ||
+      !check_tensor(dbeta, any, esz) || !check_tensor(S_in, false, 16) ||
+      !check_tensor(dS_out, false, 16) || !check_tensor(dS_in, false, 16))
+    return GDN_ERR_INVALID_ARG;
+  if (p.varlen && (!cu || !al(cu, 4))) return GDN_ERR_INVALID_ARG;
+  if (!ws || !al(ws, kAlign) || wsb < ws_bytes(p, true)) return GDN_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  SimtWs w;
+  int *blk0, *blk_seq;
+  simt_layout(p, true, &w, &blk0, &blk_seq, (char*)ws);
+  cudaError_t e;
+  if (p.varlen)
+    e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st);
+  else {
+    prof_mark(st, "status");
+    k_status_ok<<<1, 1, 0, st>>>(w.status);
+    e = cudaGetLastError();
+  }
+  if (e) return GDN_ERR_CUDA;
+  const SeqMap m = make_map(p, cu, blk0, blk_seq);
+  e = simt_bwd(m, p.dk, p.dv, p.dtype, q, k, v, g, beta, S_in, dout, dS_out, dq, dk, dv, dg,
+               dbeta, dS_in, w, st);
+  return e ? GDN_ERR_CUDA : GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_chunk_workspace_bytes(const gdn_shape* shape, int is_bwd) {
+  Plan p;
+  if (plan_shape(shape, false, 0, &p) != GDN_OK) return 0;
+  return ws_bytes(p, is_bwd != 0);
+}
+
+size_t gdn_varlen_workspace_bytes(const gdn_shape* shape, int nseq, int is_bwd) {
+  Plan p;
+  if (plan_shape(shape, true, nseq, &p) != GDN_OK) return 0;
+  return ws_bytes(p, is_bwd != 0);
+}
+
+gdn_status gdn_chunk_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* S_in, void* o,
+                         float* S_out, void* workspace, size_t workspace_bytes, void* stream) {
+  Plan p;
+  gdn_status s = plan_shape(shape, false, 0, &p);
+  if (s != GDN_OK) return s;
+  return run_fwd(p, nullptr, q, k, v, g, beta, S_in, o, S_out, workspace, workspace_bytes,
+                 stream);
+}
+
+gdn_status gdn_chunk_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* S_in, const void* dout,
+                         const float* dS_out, void* dq, void* dk, void* dv, void* dg,
+                         void* dbeta, float* dS_in, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  Plan p;
+  gdn_status s = plan_shape(shape, false, 0, &p);
+  if (s != GDN_OK) return s;
+  return run_bwd(p, nullptr, q, k, v, g, beta, S_in, dout, dS_out, dq, dk, dv, dg, dbeta, dS_in,
+                 workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_varlen_fwd(const gdn_shape* shape, const int* cu_seqlens, int nseq,
+                          const void* q, const void* k, const void* v, const void* g,
+                          const void* beta, const float* S0, void* o, float* S_final,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  Plan p;
+  gdn_status s = plan_shape(shape, true, nseq, &p);
+  if (s != GDN_OK) return s;
+  return run_fwd(p, cu_seqlens, q, k, v, g, beta, S0, o, S_final, workspace, workspace_bytes,
+                 stream);
+}
+
+gdn_status gdn_varlen_bwd(const gdn_shape* shape, const int* cu_seqlens, int nseq,
+                          const void* q, const void* k, const void* v, const void* g,
+                          const void* beta, const float* S0, const void* dout,
+                          const float* dS_final, void* dq, void* dk, void* dv, void* dg,
+                          void* dbeta, float* dS0, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  Plan p;
+  gdn_status s = plan_shape(shape, true, nseq, &p);
+  if (s != GDN_OK) return s;
+  return run_bwd(p, cu_seqlens, q, k, v, g, beta, S0, dout, dS_final, dq, dk, dv, dg, dbeta,
+                 dS0, workspace, workspace_bytes, stream);
+}
+
+const char* gdn_status_str(gdn_status status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+  }
+  return "GDN_ERR_UNKNOWN";
+}
+
+gdn_status gdn_workspace_status(void* workspace, void* stream) {
+  if (!workspace || !al(workspace, kAlign)) return GDN_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  switch (word) {
+    case DEV_OK: return GDN_OK;
+    case DEV_BAD_CU_SEQLENS: return GDN_ERR_INVALID_ARG;
+    case DEV_TIMEOUT: return GDN_ERR_TIMEOUT;
+  }
+  return GDN_ERR_CUDA;
+}
+
+int gdn_path(const gdn_shape* shape) {
+  Plan p;
+  if (plan_shape(shape, false, 0, &p) != GDN_OK) return 0;
+  return 1;
+}
+
+int gdn_version(void) { return 100; }
+
+void gdn_profile_arm(void** events, int capacity) {
+  gdn::g_prof_ev = (events && capacity > 0) ? (cudaEvent_t*)events : nullptr;
+  gdn::g_prof_cap = capacity < 4096 ? capacity : 4096;
+  gdn::g_prof_n = 0;
+}
+
+int gdn_profile_count(void) { return gdn::g_prof_n; }
+
+const char* gdn_profile_name(int i) {
+  return (i >= 0 && i < gdn::g_prof_n) ? gdn::g_prof_names[i] : nullptr;
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// Shared device-side definitions of the GDN chunk kernels: sequence/block
+// maps, workspace views and element loads. Internal to the library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Kernel-level block length: the blocks b_{i,j} inside a chunk (StateFlow
+// review, "Assumptions & free parameters"). Blocks are anchored at the start
+// of every sequence of a call, so a split at a multiple of BT leaves every
+// block, and therefore every result, unchanged.
+constexpr int BT = 64;
+
+// Where the blocks of a call live. Fixed-length calls have B sequences of T
+// tokens each (token n of sequence b is row b*T + n); varlen calls read the
+// sequence offsets from cu_seqlens and the block tables the prep kernel wrote.
+struct SeqMap {
+  const int* cu;       // varlen: device cu_seqlens [nseq + 1]; fixed: nullptr
+  const int* blk0;     // varlen: first global block of each sequence [nseq + 1]
+  const int* blk_seq;  // varlen: owning sequence of each global block (-1 = none)
+  int nseq;
+  int T_fixed;         // fixed: tokens per sequence
+  int nblk_fixed;      // fixed: blocks per sequence
+  int nblk_cap;        // global blocks launched by the per-block kernels
+  int H;
+};
+
+struct BlockInfo {
+  int seq, tok0, len, lb;
+};
+
+__device__ __forceinline__ bool block_info(const SeqMap& m, int gb, BlockInfo& bi) {
+  if (m.cu == nullptr) {
+    const int s = gb / m.nblk_fixed;
+    const int lb = gb - s * m.nblk_fixed;
+    bi.seq = s;
+    bi.lb = lb;
+    bi.tok0 = s * m.T_fixed + lb * BT;
+    bi.len = min(BT, m.T_fixed - lb * BT);
+    return bi.len > 0;
+  }
+  const int s = m.blk_seq[gb];
+  if (s < 0) return false;
+  const int lb = gb - m.blk0[s];
+  const int t0 = m.cu[s] + lb * BT;
+  bi.seq = s;
+  bi.lb = lb;
+  bi.tok0 = t0;
+  bi.len = min(BT, m.cu[s + 1] - t0);
+  return bi.len > 0;
+}
+
+struct SeqInfo {
+  int tok0, len, blk0, nblk;
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const SeqMap& m, int s) {
+  if (m.cu == nullptr) return {s * m.T_fixed, m.T_fixed, s * m.nblk_fixed, m.nblk_fixed};
+  const int t0 = m.cu[s], t1 = m.cu[s + 1];
+  const int b0 = m.blk0[s], b1 = m.blk0[s + 1];
+  if (t1 < t0 || b1 < b0) return {t0, 0, b0, 0};
+  return {t0, t1 - t0, b0, b1 - b0};
+}
+
+// Device-side status codes written into the workspace status word.
+enum : int { DEV_OK = 0, DEV_BAD_CU_SEQLENS = 1, DEV_TIMEOUT = 2 };
+
+// Workspace views (fp32 intermediates of the SIMT kernels). Indexed by
+// bh = global_block * H + head.
+struct SimtWs {
+  int* status;
+  float* gam;  // [nblk, H, BT]     block-local cumulative log-decay
+  float* W;    // [nblk, H, BT, dk] W = T diag(beta Gamma) K
+  float* U;    // [nblk, H, BT, dv] U = T diag(beta) V
+  float* Hb;   // [nblk, H, dk, dv] state at the start of the block
+  float* Vn;   // [nblk, H, BT, dv] V^new = U - W Hb
+  float* Tm;   // [nblk, H, BT, BT] T = (I + A)^-1            (backward)
+  float* dH;   // [nblk, H, dk, dv] state gradient after the block (backward)
+  float* dVn;  // [nblk, H, BT, dv] gradient of V^new      (backward)
+};
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float* p, float x) { *p = x; }
+__device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+}  // namespace gdn

@@ -1,0 +1,26 @@
+// Internal launch interface between the C-ABI host code and the kernel files.
+#pragma once
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+// fp32-arithmetic SIMT kernels (gdn_simt.cu).
+size_t simt_max_smem();
+cudaError_t simt_fwd(const SeqMap& m, int dk, int dv, int dtype, const void* q, const void* k,
+                     const void* v, const void* g, const void* beta, const float* S_in,
+                     void* o, float* S_out, const SimtWs& ws, cudaStream_t st);
+cudaError_t simt_bwd(const SeqMap& m, int dk, int dv, int dtype, const void* q, const void* k,
+                     const void* v, const void* g, const void* beta, const float* S_in,
+                     const void* dout, const float* dS_out, void* dq, void* dk_out, void* dv_out,
+                     void* dg, void* dbeta, float* dS_in, const SimtWs& ws, cudaStream_t st);
+
+// Diagnostic timing hook (include/gdn_profile.h): records an event before the
+// kernel named `next` (nullptr after the last kernel of a call) when armed.
+void prof_mark(cudaStream_t st, const char* next);
+
+// Builds the varlen block tables from device cu_seqlens (gdn_api.cu).
+cudaError_t varlen_prep(const int* cu, int nseq, int T, int nblk_cap, int* blk0, int* blk_seq,
+                        int* status, cudaStream_t st);
+
+}  // namespace gdn

@@ -1,0 +1,35 @@
+/*
+ * gdn_profile.h -- diagnostic timing hook of libgdn (not part of the compute
+ * ABI; no counterpart on the StateFlow pages).
+ *
+ * When armed, every gdn_* compute call records one caller-created CUDA event
+ * on its stream before each kernel it launches and one after the last, and
+ * remembers the kernel's name, so a benchmark can time each kernel on the
+ * stream it runs on. Disarmed (the default) it costs nothing.
+ *
+ * The hook is process-global and not thread-safe: arm it, run the calls to be
+ * timed from one thread, read the marks, disarm it. Events are owned by the
+ * caller (cudaEvent_t handles passed as void*). When the capacity is
+ * exhausted further marks are dropped and gdn_profile_count stops growing.
+ */
+#ifndef GDN_PROFILE_H_
+#define GDN_PROFILE_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Arm with `capacity` caller-created events (NULL / 0 disarms). Resets the count. */
+void gdn_profile_arm(void** events, int capacity);
+
+/* Number of marks recorded since arming. Mark i is events[i]; the kernel that
+ * ran between mark i and mark i + 1 is gdn_profile_name(i) (NULL after the
+ * last kernel of a call). */
+int gdn_profile_count(void);
+const char* gdn_profile_name(int i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_PROFILE_H_ */
