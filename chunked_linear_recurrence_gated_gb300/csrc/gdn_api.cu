@@ -112,6 +112,14 @@ gdn_status plan_shape(const gdn_shape* s, bool varlen, int nseq, Plan* p) {
   return GDN_OK;
 }
 
+// Kernel family for a shape: 2 = bf16 tensor-core kernels, 1 = fp32-arithmetic
+// SIMT kernels. Depends only on dtype, dk and dv (never on T), so chunked and
+// unchunked calls of one problem always run the same arithmetic.
+int path_of(const Plan& p) {
+  if (p.dtype == GDN_DTYPE_BF16 && p.dk == 128 && (p.dv == 128 || p.dv == 256)) return 2;
+  return 1;
+}
+
 struct Carve {
   size_t off = 0;
   size_t take(size_t bytes) {
@@ -155,9 +163,50 @@ size_t simt_layout(const Plan& p, bool bwd, SimtWs* ws, int** blk0, int** blk_se
   return c.off;
 }
 
+// Workspace layout of the tensor-core kernels (bf16 intermediates).
+size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, char* base) {
+  Carve c;
+  const size_t nbh = (size_t)p.nblk_cap * p.H;
+  const size_t o_status = c.take(kAlign);
+  const size_t o_blk0 = p.varlen ? c.take(sizeof(int) * (p.nseq + 1)) : 0;
+  const size_t o_blks = p.varlen ? c.take(sizeof(int) * (size_t)p.nblk_cap) : 0;
+  const size_t o_gam = c.take(4 * nbh * BT);
+  const size_t o_W = c.take(2 * nbh * BT * p.dk);
+  const size_t o_U = c.take(2 * nbh * BT * p.dv);
+  const size_t o_QKM = c.take(2 * nbh * BT * BT);
+  size_t o_T = 0, o_Hb = 0, o_Vn = 0, o_dH = 0, o_dVn = 0;
+  if (bwd) {
+    o_T = c.take(2 * nbh * BT * BT);
+    o_Hb = c.take(2 * nbh * p.dv * p.dk);
+    o_Vn = c.take(2 * nbh * p.dv * BT);
+    o_dH = c.take(2 * nbh * p.dv * p.dk);
+    o_dVn = c.take(2 * nbh * p.dv * BT);
+  }
+  if (base) {
+    using bf = __nv_bfloat16;
+    ws->status = (int*)(base + o_status);
+    ws->gam = (float*)(base + o_gam);
+    ws->W = (bf*)(base + o_W);
+    ws->U = (bf*)(base + o_U);
+    ws->QKM = (bf*)(base + o_QKM);
+    ws->T = bwd ? (bf*)(base + o_T) : nullptr;
+    ws->HbT = bwd ? (bf*)(base + o_Hb) : nullptr;
+    ws->VnT = bwd ? (bf*)(base + o_Vn) : nullptr;
+    ws->dHT = bwd ? (bf*)(base + o_dH) : nullptr;
+    ws->dVnT = bwd ? (bf*)(base + o_dVn) : nullptr;
+    *blk0 = p.varlen ? (int*)(base + o_blk0) : nullptr;
+    *blk_seq = p.varlen ? (int*)(base + o_blks) : nullptr;
+  }
+  return c.off;
+}
+
 size_t ws_bytes(const Plan& p, bool bwd) {
-  SimtWs w;
   int *a, *b;
+  if (path_of(p) == 2) {
+    TcWs w;
+    return tc_layout(p, bwd, &w, &a, &b, nullptr);
+  }
+  SimtWs w;
   return simt_layout(p, bwd, &w, &a, &b, nullptr);
 }
 
@@ -195,10 +244,19 @@ gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, c
   if (p.varlen && (!cu || !al(cu, 4))) return GDN_ERR_INVALID_ARG;
   if (!ws || !al(ws, kAlign) || wsb < ws_bytes(p, false)) return GDN_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
-  SimtWs w;
   int *blk0, *blk_seq;
-  simt_layout(p, false, &w, &blk0, &blk_seq, (char*)ws);
   cudaError_t e;
+  if (path_of(p) == 2) {
+    TcWs w;
+    tc_layout(p, false, &w, &blk0, &blk_seq, (char*)ws);
+    if (p.varlen && (e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st)))
+      return GDN_ERR_CUDA;
+    const SeqMap m = make_map(p, cu, blk0, blk_seq);
+    e = tc_fwd(m, p.dv, q, k, v, g, beta, S_in, o, S_out, w, st);
+    return e ? GDN_ERR_CUDA : GDN_OK;
+  }
+  SimtWs w;
+  simt_layout(p, false, &w, &blk0, &blk_seq, (char*)ws);
   if (p.varlen)
     e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st);
   else {
@@ -228,10 +286,20 @@ gdn_status run_bwd(const Plan& p, const int* cu, const void* q, const void* k, c
   if (p.varlen && (!cu || !al(cu, 4))) return GDN_ERR_INVALID_ARG;
   if (!ws || !al(ws, kAlign) || wsb < ws_bytes(p, true)) return GDN_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
-  SimtWs w;
   int *blk0, *blk_seq;
-  simt_layout(p, true, &w, &blk0, &blk_seq, (char*)ws);
   cudaError_t e;
+  if (path_of(p) == 2) {
+    TcWs w;
+    tc_layout(p, true, &w, &blk0, &blk_seq, (char*)ws);
+    if (p.varlen && (e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st)))
+      return GDN_ERR_CUDA;
+    const SeqMap m = make_map(p, cu, blk0, blk_seq);
+    if ((e = tc_bwd_prep(m, p.dv, q, k, v, g, beta, S_in, w, st))) return GDN_ERR_CUDA;
+    e = tc_bwd(m, p.dv, q, k, v, beta, dout, dS_out, dq, dk, dv, dg, dbeta, dS_in, w, st);
+    return e ? GDN_ERR_CUDA : GDN_OK;
+  }
+  SimtWs w;
+  simt_layout(p, true, &w, &blk0, &blk_seq, (char*)ws);
   if (p.varlen)
     e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st);
   else {
@@ -341,7 +409,7 @@ gdn_status gdn_workspace_status(void* workspace, void* stream) {
 int gdn_path(const gdn_shape* shape) {
   Plan p;
   if (plan_shape(shape, false, 0, &p) != GDN_OK) return 0;
-  return 1;
+  return path_of(p);
 }
 
 int gdn_version(void) { return 100; }

@@ -83,6 +83,20 @@ struct SimtWs {
   float* dVn;  // [nblk, H, BT, dv] gradient of V^new      (backward)
 };
 
+// Workspace views of the bf16 tensor-core kernels (bh = global_block * H + head).
+struct TcWs {
+  int* status;
+  float* gam;            // [nblk, H, BT]          block-local cumulative log-decay
+  __nv_bfloat16* W;      // [nblk, H, BT, 128]     W = T diag(beta Gamma) K
+  __nv_bfloat16* U;      // [nblk, H, dv/16, BT, 16]  U = T diag(beta) V, tile-major
+  __nv_bfloat16* QKM;    // [nblk, H, BT, BT]      Q K^T * Mask (j <= r)
+  __nv_bfloat16* T;      // [nblk, H, BT, BT]      (I + A)^-1          (backward)
+  __nv_bfloat16* HbT;    // [nblk, H, dv, 128]     H_b^T               (backward)
+  __nv_bfloat16* VnT;    // [nblk, H, dv, BT]      V^new^T             (backward)
+  __nv_bfloat16* dHT;    // [nblk, H, dv, 128]     dH_{b+1}^T          (backward)
+  __nv_bfloat16* dVnT;   // [nblk, H, dv, BT]      dV^new^T            (backward)
+};
+
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void stf(float* p, float x) { *p = x; }
