@@ -79,6 +79,22 @@ def kernel_model(name, dk, dv, esz=2, C=64):
         by = (C * (2 * dk + 2 * dv) * esz + 2 * C * esz + 2 * dk * dv * f4 + 2 * C * dv * f4
               + C * C * f4 + C * f4 + C * (2 * dk + dv) * esz + 2 * C * esz)
         fl = 6 * C * dk * dv + 10 * C * C * dk + 6 * C * C * dv + 4 * C ** 3
+    elif name == "tc_pre":
+        by = C * (2 * dk + dv) * esz + 2 * C * esz + C * (dk + dv) * esz + C * C * esz + C * f4
+        fl = 4 * C * C * dk + C ** 3 / 3 + 2 * C * C * dk + 2 * C * C * dv
+    elif name == "tc_chain_fwd":
+        by = C * (3 * dk + dv) * esz + C * C * esz + C * f4 + C * dv * esz
+        fl = 6 * C * dk * dv + 2 * C * C * dv
+    elif name == "tc_chain_recompute":
+        by = C * (2 * dk + dv) * esz + C * f4 + dk * dv * esz + C * dv * esz
+        fl = 4 * C * dk * dv
+    elif name == "tc_chain_bwd":
+        by = C * (3 * dk + dv) * esz + C * C * esz + C * f4 + dk * dv * esz + C * dv * esz
+        fl = 6 * C * dk * dv + 2 * C * C * dv
+    elif name == "tc_grad":
+        by = (C * (2 * dk + 2 * dv) * esz + C * esz + C * C * esz + C * f4 + 2 * dk * dv * esz
+              + 2 * C * dv * esz + C * (2 * dk + dv) * esz + 2 * C * esz)
+        fl = 6 * C * dk * dv + 4 * C * C * dv + 14 * C * C * dk + 4 * C ** 3
     else:
         return None
     return by, fl
@@ -290,11 +306,28 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
+                    help="workload index (1-3: fixed-length chunked bf16 workloads)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run only the first N tokens (a whole number of chunks); "
+                         "for small profiling cases")
     args = ap.parse_args()
+
+    import dataclasses
 
     from chunked_linear_recurrence_gated_gb300.inputs import workload
 
-    w = workload(WORKLOAD_INDEX)
+    w = workload(args.workload)
+    if args.tokens:
+        n = 0
+        acc = 0
+        while n < len(w.chunks) and acc + w.chunks[n] <= args.tokens:
+            acc += w.chunks[n]
+            n += 1
+        if n == 0:
+            raise SystemExit("--tokens is smaller than the first chunk")
+        w = dataclasses.replace(w, T=acc, chunks=w.chunks[:n],
+                                name=f"{w.name}_first{acc}")
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local = int(os.environ.get("LOCAL_RANK", 0))
