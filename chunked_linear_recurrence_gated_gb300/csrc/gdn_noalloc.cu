@@ -1,0 +1,54 @@
+// gdn_chunk_fwd_noalloc: the chunk forward with its scratch memory in a
+// fixed, library-owned device array instead of a caller-provided workspace.
+//
+// Some callers cannot hand the library a workspace: they run inside a host
+// framework that owns all device memory and exposes no allocator, or they must
+// never trigger a device allocation (which can synchronise the device) while
+// they run. This entry point serves them. Its scratch is one file-scope
+// __device__ array of GDN_NOALLOC_SCRATCH_BYTES that every GPU which loads the
+// library keeps until the process exits; the caller still passes every input
+// and output buffer.
+#include <mutex>
+
+#include "../../include/gdn.h"
+
+namespace {
+
+// Device-resident scratch shared by every call on a device.
+static __device__ __align__(256) unsigned char g_scratch[GDN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// The host-side name g_scratch is only a stand-in: kernels must be given the
+// device address, which is looked up once per device with that device current.
+gdn_status scratch_for_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_shape* shape, const void* q, const void* k,
+                                            const void* v, const void* g, const void* beta,
+                                            const float* S_in, void* o, float* S_out,
+                                            void* stream) {
+  const size_t need = gdn_chunk_workspace_bytes(shape, 0);
+  if (need == 0)  // invalid or unsupported shape: report it exactly as gdn_chunk_fwd does
+    return gdn_chunk_fwd(shape, q, k, v, g, beta, S_in, o, S_out, nullptr, 0, stream);
+  if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const gdn_status s = scratch_for_current_device(&scratch);
+  if (s != GDN_OK) return s;
+  return gdn_chunk_fwd(shape, q, k, v, g, beta, S_in, o, S_out, scratch,
+                       (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream);
+}

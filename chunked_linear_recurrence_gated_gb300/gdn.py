@@ -25,7 +25,8 @@ _STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
 
 EXPORTS = ["gdn_chunk_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "gdn_varlen_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd",
-           "gdn_status_str", "gdn_workspace_status", "gdn_path", "gdn_version"]
+           "gdn_status_str", "gdn_workspace_status", "gdn_path", "gdn_version",
+           "gdn_chunk_fwd_noalloc"]
 
 
 class GdnError(RuntimeError):
@@ -78,6 +79,8 @@ def load(build_if_missing: bool = False):
     lib.gdn_path.restype = I
     lib.gdn_version.argtypes = []
     lib.gdn_version.restype = I
+    lib.gdn_chunk_fwd_noalloc.argtypes = [SP] + [P] * 8 + [P]
+    lib.gdn_chunk_fwd_noalloc.restype = I
     lib.gdn_profile_arm.argtypes = [P, I]
     lib.gdn_profile_arm.restype = None
     lib.gdn_profile_count.argtypes = []

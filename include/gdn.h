@@ -46,7 +46,8 @@
  * -----------------------
  * The caller owns every buffer, including the workspace (size from the
  * *_workspace_bytes functions). The library allocates no device memory and
- * keeps no state between calls other than per-device kernel attributes.
+ * keeps no state between calls other than per-device kernel attributes (and
+ * the fixed scratch array of gdn_chunk_fwd_noalloc, below).
  * All work is enqueued on `stream` (a cudaStream_t passed as void*, NULL =
  * the legacy default stream); calls return without synchronising. S_out may
  * alias S_in and dS_in may alias dS_out. Other outputs must not alias
@@ -126,6 +127,26 @@ gdn_status gdn_varlen_bwd(const gdn_shape* shape, const int* cu_seqlens, int nse
                           const float* dS_final, void* dq, void* dk, void* dv, void* dg,
                           void* dbeta, float* dS0, void* workspace, size_t workspace_bytes,
                           void* stream);
+
+/* gdn_chunk_fwd without a caller-provided workspace. (No counterpart on the
+ * StateFlow pages: this serves callers that cannot allocate device memory,
+ * e.g. code running under a host framework that owns all device memory and
+ * offers no allocator, or code that must not trigger an allocation while it
+ * runs.) Arguments and results are those of gdn_chunk_fwd. The scratch is a
+ * library-owned device array of GDN_NOALLOC_SCRATCH_BYTES, held by every GPU
+ * that loads the library until the process exits; a shape whose forward
+ * workspace (gdn_chunk_workspace_bytes(shape, 0)) exceeds it is rejected with
+ * GDN_ERR_WORKSPACE before anything is launched (for dk = dv = 128 bf16 that
+ * is about 1600 blocks x heads, i.e. B * ceil(T / 64) * H <= 1600). The call
+ * allocates nothing. Its first call on a device looks up the array's device
+ * address on the current device; make that first call before any stream
+ * capture. Every call on a device shares the one array and no part of it needs
+ * to start at zero; calls whose GPU work overlaps (other streams, other host
+ * threads) race on it and must be serialised by the caller. */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+gdn_status gdn_chunk_fwd_noalloc(const gdn_shape* shape, const void* q, const void* k,
+                                 const void* v, const void* g, const void* beta,
+                                 const float* S_in, void* o, float* S_out, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* gdn_status_str(gdn_status status);
