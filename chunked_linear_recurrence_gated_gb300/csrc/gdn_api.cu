@@ -170,10 +170,10 @@ size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, c
   const size_t o_status = c.take(kAlign);
   const size_t o_blk0 = p.varlen ? c.take(sizeof(int) * (p.nseq + 1)) : 0;
   const size_t o_blks = p.varlen ? c.take(sizeof(int) * (size_t)p.nblk_cap) : 0;
-  const size_t o_gam = c.take(4 * nbh * BT);
-  const size_t o_W = c.take(2 * nbh * BT * p.dk);
-  const size_t o_U = c.take(2 * nbh * BT * p.dv);
-  const size_t o_QKM = c.take(2 * nbh * BT * BT);
+  const size_t o_dec = c.take(4 * nbh * 3 * BT);
+  const size_t o_W = c.take(2 * nbh * BT * TC_LDK);
+  const size_t o_U = c.take(2 * nbh * (p.dv / 16) * BT * TC_LDU);
+  const size_t o_QKM = c.take(2 * nbh * BT * TC_LD64);
   size_t o_T = 0, o_Hb = 0, o_Vn = 0, o_dH = 0, o_dVn = 0;
   if (bwd) {
     o_T = c.take(2 * nbh * BT * BT);
@@ -185,7 +185,7 @@ size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, c
   if (base) {
     using bf = __nv_bfloat16;
     ws->status = (int*)(base + o_status);
-    ws->gam = (float*)(base + o_gam);
+    ws->dec = (float*)(base + o_dec);
     ws->W = (bf*)(base + o_W);
     ws->U = (bf*)(base + o_U);
     ws->QKM = (bf*)(base + o_QKM);

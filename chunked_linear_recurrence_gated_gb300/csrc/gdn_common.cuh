@@ -84,12 +84,17 @@ struct SimtWs {
 };
 
 // Workspace views of the bf16 tensor-core kernels (bh = global_block * H + head).
+// Pre writes W, U and QKM with padded rows so that each lands in the chain's
+// padded shared-memory tiles with a single bulk copy.
+constexpr int TC_LDK = 136;   // padded row of 128-wide bf16 tiles
+constexpr int TC_LD64 = 72;   // padded row of 64-wide bf16 tiles
+constexpr int TC_LDU = 24;    // padded row of a 16-column U tile
 struct TcWs {
   int* status;
-  float* gam;            // [nblk, H, BT]          block-local cumulative log-decay
-  __nv_bfloat16* W;      // [nblk, H, BT, 128]     W = T diag(beta Gamma) K
-  __nv_bfloat16* U;      // [nblk, H, dv/16, BT, 16]  U = T diag(beta) V, tile-major
-  __nv_bfloat16* QKM;    // [nblk, H, BT, BT]      Q K^T * Mask (j <= r)
+  float* dec;            // [nblk, H, 3, BT]   Gamma_r, e^{gamma_C - gamma_r}, gamma_r
+  __nv_bfloat16* W;      // [nblk, H, BT, TC_LDK]          W = T diag(beta Gamma) K
+  __nv_bfloat16* U;      // [nblk, H, dv/16, BT, TC_LDU]   U = T diag(beta) V, tile-major
+  __nv_bfloat16* QKM;    // [nblk, H, BT, TC_LD64]         Q K^T * Mask (j <= r)
   __nv_bfloat16* T;      // [nblk, H, BT, BT]      (I + A)^-1          (backward)
   __nv_bfloat16* HbT;    // [nblk, H, dv, 128]     H_b^T               (backward)
   __nv_bfloat16* VnT;    // [nblk, H, dv, BT]      V^new^T             (backward)

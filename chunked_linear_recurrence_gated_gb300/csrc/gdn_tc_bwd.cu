@@ -14,196 +14,258 @@
 namespace gdn {
 namespace {
 
-constexpr int LDK = 136;
-constexpr int LD64 = 72;
+constexpr int LDK = TC_LDK;
+constexpr int LD64 = TC_LD64;
 constexpr int NSTAGE = 3;
 
 // ------------------------------------------------------------------ reverse chain
+// Same structure as the forward chain: 4 compute warps carry dH^T (16 value
+// rows x 128 key columns, fp32, warp w owns key columns [32w, 32w + 32)); one
+// producer warp fills a 3-stage ring with bulk copies of W, QKM, decay factors
+// (workspace) and K, Q, dO rows (inputs), visiting the blocks last to first.
 struct RevStage {
   __nv_bfloat16 W[BT * LDK];
   __nv_bfloat16 K[BT * LDK];
   __nv_bfloat16 Q[BT * LDK];
   __nv_bfloat16 QKM[BT * LD64];
   __nv_bfloat16 dO[BT * 24];
-  float g[BT];
+  float dec[3 * BT];
 };
 
 struct RevSmem {
   RevStage st[NSTAGE];
+  uint64_t full[NSTAGE];
+  uint64_t empty[NSTAGE];
   __nv_bfloat16 dHT[16 * LDK];   // bf16 copy of dH^T (value rows)
   __nv_bfloat16 dVT[16 * LD64];  // -dV^new^T (value rows)
   __nv_bfloat16 dOs[BT * 24];    // diag(Gamma) dO tile
+  int abort;
 };
 
+constexpr int REV_THREADS = 160;
+
 template <int DV>
-__global__ void __launch_bounds__(128, 1) k_chain_bwd(SeqMap m, const __nv_bfloat16* __restrict__ q,
-                                                      const __nv_bfloat16* __restrict__ k,
-                                                      const __nv_bfloat16* __restrict__ dout,
-                                                      const float* dS_out, float* dS_in, TcWs ws) {
+__global__ void __launch_bounds__(REV_THREADS, 1)
+    k_chain_bwd(SeqMap m, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                const __nv_bfloat16* __restrict__ dout, const float* dS_out, float* dS_in,
+                TcWs ws) {
   constexpr int DK = 128;
   constexpr int NVT = DV / 16;
+  constexpr int NS = NSTAGE;
   const int tile = blockIdx.x % NVT;
   const int sh = blockIdx.x / NVT;
   const int H = m.H, h = sh % H, s = sh / H;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
   const SeqInfo si = seq_info(m, s);
-  extern __shared__ __align__(16) unsigned char smraw[];
+  extern __shared__ __align__(128) unsigned char smraw[];
   RevSmem& sm = *reinterpret_cast<RevSmem*>(smraw);
+  volatile int* abort = &sm.abort;
 
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&sm.full[i], 1 + 32);  // bulk-copy arrival + one cp.async arrival per producer lane
+      mbar_init(&sm.empty[i], 4);
+    }
+    sm.abort = 0;
+    fence_mbar_init();
+  }
   float dh[4][4];
   const size_t sbase = ((size_t)s * H + h) * DK * DV + (size_t)tile * 16;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int vr = gq + 8 * (e >> 1);
-      const int kc = 32 * w + 8 * j + 2 * tq + (e & 1);
-      dh[j][e] = dS_out ? dS_out[sbase + (size_t)kc * DV + vr] : 0.f;
-    }
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int vr = gq + 8 * hf, kc = 32 * w + 8 * j + 2 * tq;
-      *reinterpret_cast<uint32_t*>(&sm.dHT[vr * LDK + kc]) = pack_bf16(dh[j][2 * hf], dh[j][2 * hf + 1]);
-    }
-
-  auto load_block = [&](int lb) {
-    RevStage& S = sm.st[lb % NSTAGE];
-    const int gb = si.blk0 + lb, tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
-    const size_t bh = (size_t)gb * H + h;
-    const __nv_bfloat16* Wg = ws.W + bh * BT * DK;
-    for (int idx = tid; idx < BT * 16; idx += 128) {
-      const int r = idx >> 4, c = (idx & 15) * 8;
-      const bool ok = r < len;
-      const size_t off = ((size_t)(tok0 + (ok ? r : 0)) * H + h) * DK + c;
-      cp16(&S.W[r * LDK + c], Wg + r * DK + c, true);
-      cp16(&S.K[r * LDK + c], k + off, ok);
-      cp16(&S.Q[r * LDK + c], q + off, ok);
-    }
-    const __nv_bfloat16* Mg = ws.QKM + bh * BT * BT;
-    for (int idx = tid; idx < BT * 8; idx += 128) {
-      const int r = idx >> 3, c = (idx & 7) * 8;
-      cp16(&S.QKM[r * LD64 + c], Mg + r * BT + c, true);
-    }
-    {
-      const int r = tid >> 1, c = (tid & 1) * 8;
-      const bool ok = r < len;
-      cp16(&S.dO[r * 24 + c], dout + ((size_t)(tok0 + (ok ? r : 0)) * H + h) * DV + tile * 16 + c, ok);
-    }
-    if (tid < 16) cp16(&S.g[tid * 4], ws.gam + bh * BT + tid * 4, true);
-  };
-
-  // blocks are visited from the last to the first: stage i holds block nblk-1-i
-#pragma unroll
-  for (int i = 0; i < NSTAGE - 1; ++i) {
-    if (i < si.nblk) load_block(si.nblk - 1 - i);
-    cp_commit();
-  }
-  for (int it = 0; it < si.nblk; ++it) {
-    const int lb = si.nblk - 1 - it;
-    cp_wait<NSTAGE - 2>();
-    __syncthreads();
-    if (it + NSTAGE - 1 < si.nblk) load_block(si.nblk - 1 - (it + NSTAGE - 1));
-    cp_commit();
-    const RevStage& S = sm.st[lb % NSTAGE];
-    const int gb = si.blk0 + lb;
-    const size_t bh = (size_t)gb * H + h;
-    const float gC = S.g[BT - 1];
-
-    // dH_{b+1} (bf16, value-major) for the gradient kernel
-    {
-      __nv_bfloat16* Dg = ws.dHT + bh * DV * DK + (size_t)tile * 16 * DK;
-      for (int idx = tid; idx < 16 * 16; idx += 128) {
-        const int r = idx >> 4, c = (idx & 15) * 8;
-        *reinterpret_cast<uint4*>(Dg + r * DK + c) = *reinterpret_cast<const uint4*>(&sm.dHT[r * LDK + c]);
-      }
-    }
-    // diag(Gamma) dO for the off-chain term (warp w: rows 16w..16w+15)
-    {
-      const int r = 16 * w + (l >> 1), c = (l & 1) * 8;
-      const float G = expf(S.g[r]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        sm.dOs[r * 24 + c + e] = __float2bfloat16_rn(G * __bfloat162float(S.dO[r * 24 + c + e]));
-    }
-    // dV^new^T for tokens [16w, 16w + 16): dO^T QKM + (dH^T K^T) * e^{gamma_C - gamma}
-    float a1[2][4], a2[2][4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) a1[j][e] = a2[j][e] = 0.f;
-#pragma unroll
-    for (int kc = 0; kc < DK / 16; ++kc) {
-      uint32_t a[4], b[4];
-      lda_rm(a, sm.dHT, LDK, 0, 16 * kc);
-      ldb_nk_x2n(b, S.K, LDK, 16 * w, 16 * kc);
-      mma16816(a2[0], a, b[0], b[1]);
-      mma16816(a2[1], a, b[2], b[3]);
-    }
-#pragma unroll
-    for (int kc = 0; kc < 4; ++kc) {
-      uint32_t a[4], b[4];
-      lda_tr(a, S.dO, 24, 0, 16 * kc);
-      ldb_kn_x2n(b, S.QKM, LD64, 16 * kc, 16 * w);
-      mma16816(a1[0], a, b[0], b[1]);
-      mma16816(a1[1], a, b[2], b[3]);
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int vr = gq + 8 * hf;
-        const int t0 = 16 * w + 8 * j + 2 * tq;
-        const float d0 = a1[j][2 * hf] + expf(gC - S.g[t0]) * a2[j][2 * hf];
-        const float d1 = a1[j][2 * hf + 1] + expf(gC - S.g[t0 + 1]) * a2[j][2 * hf + 1];
-        *reinterpret_cast<uint32_t*>(&sm.dVT[vr * LD64 + t0]) = pack_bf16(-d0, -d1);
-        *reinterpret_cast<uint32_t*>(ws.dVnT + bh * DV * BT + (size_t)(tile * 16 + vr) * BT + t0) =
-            pack_bf16(d0, d1);
-      }
-    __syncthreads();
-    // dH^T <- Gamma_C dH^T + (Gamma dO)^T Q - dV^new^T W on key columns [32w, 32w + 32)
-    const float GC = expf(gC);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) dh[j][e] *= GC;
-#pragma unroll
-    for (int kc = 0; kc < 4; ++kc) {
-      uint32_t a[4], b[4];
-      lda_tr(a, sm.dOs, 24, 0, 16 * kc);
-      ldb_kn_x2n(b, S.Q, LDK, 16 * kc, 32 * w);
-      mma16816(dh[0], a, b[0], b[1]);
-      mma16816(dh[1], a, b[2], b[3]);
-      ldb_kn_x2n(b, S.Q, LDK, 16 * kc, 32 * w + 16);
-      mma16816(dh[2], a, b[0], b[1]);
-      mma16816(dh[3], a, b[2], b[3]);
-      lda_rm(a, sm.dVT, LD64, 0, 16 * kc);
-      ldb_kn_x2n(b, S.W, LDK, 16 * kc, 32 * w);
-      mma16816(dh[0], a, b[0], b[1]);
-      mma16816(dh[1], a, b[2], b[3]);
-      ldb_kn_x2n(b, S.W, LDK, 16 * kc, 32 * w + 16);
-      mma16816(dh[2], a, b[0], b[1]);
-      mma16816(dh[3], a, b[2], b[3]);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int vr = gq + 8 * hf, kc = 32 * w + 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(&sm.dHT[vr * LDK + kc]) = pack_bf16(dh[j][2 * hf], dh[j][2 * hf + 1]);
-      }
-  }
-  if (dS_in) {
+  if (w < 4) {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int vr = gq + 8 * (e >> 1);
         const int kc = 32 * w + 8 * j + 2 * tq + (e & 1);
-        dS_in[sbase + (size_t)kc * DV + vr] = dh[j][e];
+        dh[j][e] = dS_out ? dS_out[sbase + (size_t)kc * DV + vr] : 0.f;
+      }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int vr = gq + 8 * hf, kc = 32 * w + 8 * j + 2 * tq;
+        *reinterpret_cast<uint32_t*>(&sm.dHT[vr * LDK + kc]) =
+            pack_bf16(dh[j][2 * hf], dh[j][2 * hf + 1]);
       }
   }
+  __syncthreads();
+
+  if (w == 4) {
+    // ---------------- producer warp: iteration it loads block nblk - 1 - it
+    int issued = 0;
+    for (int it = 0; it < si.nblk; ++it) {
+      const int st = it % NS, kf = it / NS;
+      if (it >= NS && !mbar_wait(&sm.empty[st], (kf - 1) & 1, abort)) break;
+      RevStage& S = sm.st[st];
+      const int lb = si.nblk - 1 - it;
+      const int gb = si.blk0 + lb, tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
+      const size_t bh = (size_t)gb * H + h;
+      const uint32_t bytes = BT * LDK * 2 + BT * LD64 * 2 + 3 * BT * 4;
+      if (l == 0) {
+        mbar_arrive_expect_tx(&sm.full[st], bytes);
+        bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, &sm.full[st]);
+        bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, &sm.full[st]);
+        bulk_g2s(S.dec, ws.dec + bh * 3 * BT, 3 * BT * 4, &sm.full[st]);
+      }
+      // K, Q and dO rows: 16-byte cp.async per lane, rows past the block's end zero-filled
+#pragma unroll 4
+      for (int idx = l; idx < BT * (DK / 8); idx += 32) {
+        const int r = idx >> 4, c = (idx & 15) * 8;
+        const bool okr = r < len;
+        const size_t tok = (size_t)(tok0 + (okr ? r : 0)) * H + h;
+        cp16(&S.K[r * LDK + c], k + tok * DK + c, okr);
+        cp16(&S.Q[r * LDK + c], q + tok * DK + c, okr);
+      }
+#pragma unroll
+      for (int idx = l; idx < BT * 2; idx += 32) {
+        const int r = idx >> 1, c = (idx & 1) * 8;
+        const bool okr = r < len;
+        const size_t tok = (size_t)(tok0 + (okr ? r : 0)) * H + h;
+        cp16(&S.dO[r * 24 + c], dout + tok * DV + tile * 16 + c, okr);
+      }
+      cp_async_mbar_arrive(&sm.full[st]);
+      ++issued;
+    }
+    cp_wait<0>();  // this lane's own row copies
+    __syncwarp();
+    if (*abort && l == 0) {
+      for (int it = max(0, issued - NS); it < issued; ++it) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&sm.full[it % NS], (it / NS) & 1) && clock64() - t0 < (1ll << 31)) {
+        }
+      }
+    }
+  } else {
+    // ---------------- compute warps
+    for (int it = 0; it < si.nblk; ++it) {
+      const int st = it % NS;
+      const bool ok = mbar_wait(&sm.full[st], (it / NS) & 1, abort);
+      const RevStage& S = sm.st[st];
+      const int lb = si.nblk - 1 - it;
+      const size_t bh = (size_t)(si.blk0 + lb) * H + h;
+      const float* dec = S.dec;
+      // dH_{b+1} (bf16, value-major) for the gradient kernel
+      if (ok) {
+        __nv_bfloat16* Dg = ws.dHT + bh * DV * DK + (size_t)tile * 16 * DK;
+        for (int idx = tid; idx < 16 * 16; idx += 128) {
+          const int r = idx >> 4, c = (idx & 15) * 8;
+          *reinterpret_cast<uint4*>(Dg + r * DK + c) =
+              *reinterpret_cast<const uint4*>(&sm.dHT[r * LDK + c]);
+        }
+      }
+      // diag(Gamma) dO for the off-chain term (warp w: rows 16w..16w+15)
+      {
+        const int r = 16 * w + (l >> 1), c = (l & 1) * 8;
+        const float G = dec[r];
+        const uint4 raw = *reinterpret_cast<const uint4*>(&S.dO[r * 24 + c]);
+        const uint32_t* pr = reinterpret_cast<const uint32_t*>(&raw);
+        uint4 outv;
+        uint32_t* po = reinterpret_cast<uint32_t*>(&outv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack_bf16(pr[e]);
+          po[e] = pack_bf16(G * f.x, G * f.y);
+        }
+        *reinterpret_cast<uint4*>(&sm.dOs[r * 24 + c]) = outv;
+      }
+      // dV^new^T for tokens [16w, 16w + 16): dO^T QKM + (dH^T K^T) * e^{gamma_C - gamma}
+      float a1[2][2][4], a2[2][2][4];
+#pragma unroll
+      for (int p = 0; p < 2; ++p)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a1[p][j][e] = a2[p][j][e] = 0.f;
+#pragma unroll
+      for (int kc = 0; kc < DK / 16; ++kc) {
+        uint32_t a[4], b[4];
+        lda_rm(a, sm.dHT, LDK, 0, 16 * kc);
+        ldb_nk_x2n(b, S.K, LDK, 16 * w, 16 * kc);
+        mma16816(a2[kc & 1][0], a, b[0], b[1]);
+        mma16816(a2[kc & 1][1], a, b[2], b[3]);
+      }
+#pragma unroll
+      for (int kc = 0; kc < 4; ++kc) {
+        uint32_t a[4], b[4];
+        lda_tr(a, S.dO, 24, 0, 16 * kc);
+        ldb_kn_x2n(b, S.QKM, LD64, 16 * kc, 16 * w);
+        mma16816(a1[kc & 1][0], a, b[0], b[1]);
+        mma16816(a1[kc & 1][1], a, b[2], b[3]);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int vr = gq + 8 * hf;
+          const int t0 = 16 * w + 8 * j + 2 * tq;
+          const float d0 = a1[0][j][2 * hf] + a1[1][j][2 * hf] +
+                           dec[BT + t0] * (a2[0][j][2 * hf] + a2[1][j][2 * hf]);
+          const float d1 = a1[0][j][2 * hf + 1] + a1[1][j][2 * hf + 1] +
+                           dec[BT + t0 + 1] * (a2[0][j][2 * hf + 1] + a2[1][j][2 * hf + 1]);
+          *reinterpret_cast<uint32_t*>(&sm.dVT[vr * LD64 + t0]) = pack_bf16(-d0, -d1);
+          if (ok)
+            *reinterpret_cast<uint32_t*>(ws.dVnT + bh * DV * BT + (size_t)(tile * 16 + vr) * BT + t0) =
+                pack_bf16(d0, d1);
+        }
+      named_bar(1, 128);
+      // dH^T <- Gamma_C dH^T + (Gamma dO)^T Q - dV^new^T W on key columns [32w, 32w + 32)
+      const float GC = dec[BT - 1];
+      float d2[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          dh[j][e] *= GC;
+          d2[j][e] = 0.f;
+        }
+#pragma unroll
+      for (int kc = 0; kc < 4; ++kc) {
+        uint32_t a[4], b[4];
+        lda_tr(a, sm.dOs, 24, 0, 16 * kc);
+        ldb_kn_x2n(b, S.Q, LDK, 16 * kc, 32 * w);
+        mma16816(dh[0], a, b[0], b[1]);
+        mma16816(dh[1], a, b[2], b[3]);
+        ldb_kn_x2n(b, S.Q, LDK, 16 * kc, 32 * w + 16);
+        mma16816(dh[2], a, b[0], b[1]);
+        mma16816(dh[3], a, b[2], b[3]);
+        lda_rm(a, sm.dVT, LD64, 0, 16 * kc);
+        ldb_kn_x2n(b, S.W, LDK, 16 * kc, 32 * w);
+        mma16816(d2[0], a, b[0], b[1]);
+        mma16816(d2[1], a, b[2], b[3]);
+        ldb_kn_x2n(b, S.W, LDK, 16 * kc, 32 * w + 16);
+        mma16816(d2[2], a, b[0], b[1]);
+        mma16816(d2[3], a, b[2], b[3]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dh[j][e] += d2[j][e];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int vr = gq + 8 * hf, kc = 32 * w + 8 * j + 2 * tq;
+          *reinterpret_cast<uint32_t*>(&sm.dHT[vr * LDK + kc]) =
+              pack_bf16(dh[j][2 * hf], dh[j][2 * hf + 1]);
+        }
+      __syncwarp();
+      if (l == 0) mbar_arrive(&sm.empty[st]);
+      named_bar(1, 128);
+    }
+    if (dS_in && !*abort) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int vr = gq + 8 * (e >> 1);
+          const int kc = 32 * w + 8 * j + 2 * tq + (e & 1);
+          dS_in[sbase + (size_t)kc * DV + vr] = dh[j][e];
+        }
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && *abort) ws.status[0] = DEV_TIMEOUT;
 }
 
 // ------------------------------------------------------------------ per-block gradients
@@ -263,7 +325,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
   BlockInfo bi;
   const int gb = blockIdx.x, h = blockIdx.y, H = m.H, tid = threadIdx.x;
   if (!block_info(m, gb, bi)) return;
-  extern __shared__ __align__(16) unsigned char smraw[];
+  extern __shared__ __align__(128) unsigned char smraw[];
   GradSmem& sm = *reinterpret_cast<GradSmem*>(smraw);
   const int w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
   const int rw = w & 3, cw = w >> 2;
@@ -284,7 +346,10 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
   cp_commit();
   if (tid < BT) {
     const bool ok = tid < bi.len;
-    sm.g[tid] = ws.gam[bh * BT + tid];
+    const float* dec = ws.dec + bh * 3 * BT;
+    sm.G[tid] = dec[tid];
+    sm.dte[tid] = dec[BT + tid];
+    sm.g[tid] = dec[2 * BT + tid];
     sm.b[tid] = ok ? __bfloat162float(beta[(size_t)(bi.tok0 + tid) * H + h]) : 0.f;
   }
   for (int idx = tid; idx < 2 * BT; idx += 256) {
@@ -294,10 +359,6 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
   }
   for (int idx = tid; idx < 4 * BT; idx += 256) (&sm.colacc[0][0])[idx] = 0.f;
   __syncthreads();
-  if (tid < BT) {
-    sm.G[tid] = expf(sm.g[tid]);
-    sm.dte[tid] = expf(sm.g[BT - 1] - sm.g[tid]);
-  }
 
   // ---- value-dimension reductions
   float aOH[8][4], aHW[8][4], aKt[8][4], aOV[4][4], aWV[4][4];
@@ -466,7 +527,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int r = R0 + gq + 8 * (e >> 1), c = 32 * cw + 8 * j + 2 * tq + (e & 1);
-      const float msk = (c <= r) ? expf(sm.g[r] - sm.g[c]) : 0.f;
+      const float msk = (c <= r) ? __expf(sm.g[r] - sm.g[c]) : 0.f;
       sm.P[r * LD64 + c] = __float2bfloat16_rn(aOV[j][e] * msk);
       aOV[j][e] *= msk;  // P in fp32
       dT[j][e] = sm.b[c] * aWV[j][e];
@@ -632,7 +693,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       for (int e = 0; e < 4; ++e) {
         const int r = R0 + gq + 8 * (e >> 1), c = 32 * cw + 8 * j + 2 * tq + (e & 1);
         const float dA = (c < r) ? -da[j][e] : 0.f;
-        const float E = (c < r) ? dA * expf(sm.g[r] - sm.g[c]) : 0.f;
+        const float E = (c < r) ? dA * __expf(sm.g[r] - sm.g[c]) : 0.f;
         const float Gv = sm.b[r] * E * kk[j][e];
         if (e < 2) {
           pb0 += E * kk[j][e];
@@ -713,7 +774,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       dgam[hh] = sm.rowacc[0][r] + sm.rowacc[1][r] - sm.colacc[0][r] - sm.colacc[1][r] -
                  sm.colacc[2][r] - sm.colacc[3][r] - sm.rho[0][r] - sm.rho[1][r];
     }
-    if (l == 31) dgam[1] += rho + expf(sm.g[BT - 1]) * hs;
+    if (l == 31) dgam[1] += rho + sm.G[BT - 1] * hs;
     // reverse inclusive cumsum over 64 rows (fixed order)
     float a = dgam[1], c = dgam[0];
 #pragma unroll
@@ -757,7 +818,7 @@ cudaError_t tc_bwd_t(const SeqMap& m, const void* q, const void* k, const void* 
   if ((e = set_smem(k_chain_bwd<DV>, sizeof(RevSmem)))) return e;
   if ((e = set_smem(k_grad_tc<DV>, sizeof(GradSmem)))) return e;
   prof_mark(st, "tc_chain_bwd");
-  k_chain_bwd<DV><<<m.nseq * m.H * (DV / 16), 128, sizeof(RevSmem), st>>>(
+  k_chain_bwd<DV><<<m.nseq * m.H * (DV / 16), REV_THREADS, sizeof(RevSmem), st>>>(
       m, (const bf*)q, (const bf*)k, (const bf*)dout, dS_out, dS_in, ws);
   if (m.nblk_cap > 0) {
     prof_mark(st, "tc_grad");
