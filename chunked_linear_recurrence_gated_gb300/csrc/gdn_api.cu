@@ -174,6 +174,8 @@ size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, c
   const size_t o_W = c.take(2 * nbh * BT * TC_LDK);
   const size_t o_U = c.take(2 * nbh * (p.dv / 16) * BT * TC_LDU);
   const size_t o_QKM = c.take(2 * nbh * BT * TC_LD64);
+  const size_t o_Kp = c.take(2 * nbh * BT * TC_LDK);
+  const size_t o_Qp = c.take(2 * nbh * BT * TC_LDK);
   size_t o_T = 0, o_Hb = 0, o_Vn = 0, o_dH = 0, o_dVn = 0;
   if (bwd) {
     o_T = c.take(2 * nbh * BT * BT);
@@ -189,6 +191,8 @@ size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, c
     ws->W = (bf*)(base + o_W);
     ws->U = (bf*)(base + o_U);
     ws->QKM = (bf*)(base + o_QKM);
+    ws->Kp = (bf*)(base + o_Kp);
+    ws->Qp = (bf*)(base + o_Qp);
     ws->T = bwd ? (bf*)(base + o_T) : nullptr;
     ws->HbT = bwd ? (bf*)(base + o_Hb) : nullptr;
     ws->VnT = bwd ? (bf*)(base + o_Vn) : nullptr;

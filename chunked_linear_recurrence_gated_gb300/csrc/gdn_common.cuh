@@ -95,6 +95,8 @@ struct TcWs {
   __nv_bfloat16* W;      // [nblk, H, BT, TC_LDK]          W = T diag(beta Gamma) K
   __nv_bfloat16* U;      // [nblk, H, dv/16, BT, TC_LDU]   U = T diag(beta) V, tile-major
   __nv_bfloat16* QKM;    // [nblk, H, BT, TC_LD64]         Q K^T * Mask (j <= r)
+  __nv_bfloat16* Kp;     // [nblk, H, BT, TC_LDK]          K rows (padded copy, zero past the end)
+  __nv_bfloat16* Qp;     // [nblk, H, BT, TC_LDK]          Q rows (padded copy, zero past the end)
   __nv_bfloat16* T;      // [nblk, H, BT, BT]      (I + A)^-1          (backward)
   __nv_bfloat16* HbT;    // [nblk, H, dv, 128]     H_b^T               (backward)
   __nv_bfloat16* VnT;    // [nblk, H, dv, BT]      V^new^T             (backward)

@@ -101,22 +101,17 @@ __global__ void __launch_bounds__(REV_THREADS, 1)
       const int lb = si.nblk - 1 - it;
       const int gb = si.blk0 + lb, tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
       const size_t bh = (size_t)gb * H + h;
-      const uint32_t bytes = BT * LDK * 2 + BT * LD64 * 2 + 3 * BT * 4;
+      const uint32_t bytes = 3 * BT * LDK * 2 + BT * LD64 * 2 + 3 * BT * 4;
       if (l == 0) {
-        mbar_arrive_expect_tx(&sm.full[st], bytes);
-        bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, &sm.full[st]);
-        bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, &sm.full[st]);
-        bulk_g2s(S.dec, ws.dec + bh * 3 * BT, 3 * BT * 4, &sm.full[st]);
+        uint64_t* fb = &sm.full[st];
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.K, ws.Kp + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, fb);
+        bulk_g2s(S.dec, ws.dec + bh * 3 * BT, 3 * BT * 4, fb);
       }
-      // K, Q and dO rows: 16-byte cp.async per lane, rows past the block's end zero-filled
-#pragma unroll 4
-      for (int idx = l; idx < BT * (DK / 8); idx += 32) {
-        const int r = idx >> 4, c = (idx & 15) * 8;
-        const bool okr = r < len;
-        const size_t tok = (size_t)(tok0 + (okr ? r : 0)) * H + h;
-        cp16(&S.K[r * LDK + c], k + tok * DK + c, okr);
-        cp16(&S.Q[r * LDK + c], q + tok * DK + c, okr);
-      }
+      // the 16-column dO tile: 16-byte cp.async per lane, rows past the block's end zero-filled
 #pragma unroll
       for (int idx = l; idx < BT * 2; idx += 32) {
         const int r = idx >> 1, c = (idx & 1) * 8;
@@ -170,6 +165,7 @@ __global__ void __launch_bounds__(REV_THREADS, 1)
         *reinterpret_cast<uint4*>(&sm.dOs[r * 24 + c]) = outv;
       }
       // dV^new^T for tokens [16w, 16w + 16): dO^T QKM + (dH^T K^T) * e^{gamma_C - gamma}
+      // (fragments are loaded ahead of the MMAs; even / odd k-steps accumulate separately)
       float a1[2][2][4], a2[2][2][4];
 #pragma unroll
       for (int p = 0; p < 2; ++p)
@@ -177,21 +173,28 @@ __global__ void __launch_bounds__(REV_THREADS, 1)
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) a1[p][j][e] = a2[p][j][e] = 0.f;
+      {
+        uint32_t aD[DK / 16][4], bK[DK / 16][4];
 #pragma unroll
-      for (int kc = 0; kc < DK / 16; ++kc) {
-        uint32_t a[4], b[4];
-        lda_rm(a, sm.dHT, LDK, 0, 16 * kc);
-        ldb_nk_x2n(b, S.K, LDK, 16 * w, 16 * kc);
-        mma16816(a2[kc & 1][0], a, b[0], b[1]);
-        mma16816(a2[kc & 1][1], a, b[2], b[3]);
-      }
+        for (int kc = 0; kc < DK / 16; ++kc) {
+          lda_rm(aD[kc], sm.dHT, LDK, 0, 16 * kc);
+          ldb_nk_x2n(bK[kc], S.K, LDK, 16 * w, 16 * kc);
+        }
 #pragma unroll
-      for (int kc = 0; kc < 4; ++kc) {
-        uint32_t a[4], b[4];
-        lda_tr(a, S.dO, 24, 0, 16 * kc);
-        ldb_kn_x2n(b, S.QKM, LD64, 16 * kc, 16 * w);
-        mma16816(a1[kc & 1][0], a, b[0], b[1]);
-        mma16816(a1[kc & 1][1], a, b[2], b[3]);
+        for (int kc = 0; kc < DK / 16; ++kc) {
+          mma16816(a2[kc & 1][0], aD[kc], bK[kc][0], bK[kc][1]);
+          mma16816(a2[kc & 1][1], aD[kc], bK[kc][2], bK[kc][3]);
+        }
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+          lda_tr(aD[kc], S.dO, 24, 0, 16 * kc);
+          ldb_kn_x2n(bK[kc], S.QKM, LD64, 16 * kc, 16 * w);
+        }
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+          mma16816(a1[kc & 1][0], aD[kc], bK[kc][0], bK[kc][1]);
+          mma16816(a1[kc & 1][1], aD[kc], bK[kc][2], bK[kc][3]);
+        }
       }
 #pragma unroll
       for (int j = 0; j < 2; ++j)
@@ -208,6 +211,15 @@ __global__ void __launch_bounds__(REV_THREADS, 1)
             *reinterpret_cast<uint32_t*>(ws.dVnT + bh * DV * BT + (size_t)(tile * 16 + vr) * BT + t0) =
                 pack_bf16(d0, d1);
         }
+      // operands that do not depend on dV^new: load before the barrier
+      uint32_t bQ[4][8], bW[4][8];
+#pragma unroll
+      for (int kc = 0; kc < 4; ++kc) {
+        ldb_kn_x2n(&bQ[kc][0], S.Q, LDK, 16 * kc, 32 * w);
+        ldb_kn_x2n(&bQ[kc][4], S.Q, LDK, 16 * kc, 32 * w + 16);
+        ldb_kn_x2n(&bW[kc][0], S.W, LDK, 16 * kc, 32 * w);
+        ldb_kn_x2n(&bW[kc][4], S.W, LDK, 16 * kc, 32 * w + 16);
+      }
       named_bar(1, 128);
       // dH^T <- Gamma_C dH^T + (Gamma dO)^T Q - dV^new^T W on key columns [32w, 32w + 32)
       const float GC = dec[BT - 1];
@@ -219,23 +231,20 @@ __global__ void __launch_bounds__(REV_THREADS, 1)
           dh[j][e] *= GC;
           d2[j][e] = 0.f;
         }
+      {
+        uint32_t aO[4][4], aV[4][4];
 #pragma unroll
-      for (int kc = 0; kc < 4; ++kc) {
-        uint32_t a[4], b[4];
-        lda_tr(a, sm.dOs, 24, 0, 16 * kc);
-        ldb_kn_x2n(b, S.Q, LDK, 16 * kc, 32 * w);
-        mma16816(dh[0], a, b[0], b[1]);
-        mma16816(dh[1], a, b[2], b[3]);
-        ldb_kn_x2n(b, S.Q, LDK, 16 * kc, 32 * w + 16);
-        mma16816(dh[2], a, b[0], b[1]);
-        mma16816(dh[3], a, b[2], b[3]);
-        lda_rm(a, sm.dVT, LD64, 0, 16 * kc);
-        ldb_kn_x2n(b, S.W, LDK, 16 * kc, 32 * w);
-        mma16816(d2[0], a, b[0], b[1]);
-        mma16816(d2[1], a, b[2], b[3]);
-        ldb_kn_x2n(b, S.W, LDK, 16 * kc, 32 * w + 16);
-        mma16816(d2[2], a, b[0], b[1]);
-        mma16816(d2[3], a, b[2], b[3]);
+        for (int kc = 0; kc < 4; ++kc) {
+          lda_tr(aO[kc], sm.dOs, 24, 0, 16 * kc);
+          lda_rm(aV[kc], sm.dVT, LD64, 0, 16 * kc);
+        }
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma16816(dh[j], aO[kc], bQ[kc][2 * j], bQ[kc][2 * j + 1]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma16816(d2[j], aV[kc], bW[kc][2 * j], bW[kc][2 * j + 1]);
+        }
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j)

@@ -148,6 +148,17 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
   block_cumsum64(sm.g);
   cp_wait<0>();
   __syncthreads();
+  // padded copies of K and Q for the chains (one bulk copy each per block)
+  {
+    const uint4* sK = reinterpret_cast<const uint4*>(sm.K);
+    const uint4* sQ = reinterpret_cast<const uint4*>(sm.Q);
+    uint4* gK = reinterpret_cast<uint4*>(ws.Kp + bh * BT * LDK);
+    uint4* gQ = reinterpret_cast<uint4*>(ws.Qp + bh * BT * LDK);
+    for (int idx = tid; idx < BT * LDK / 8; idx += NT) {
+      gK[idx] = sK[idx];
+      gQ[idx] = sQ[idx];
+    }
+  }
   if (tid < BT) {
     const float gr = sm.g[tid];
     const float G = __expf(gr), dte = __expf(sm.g[BT - 1] - gr);
@@ -334,7 +345,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&sm.full[i], 1 + 32);  // bulk-copy arrival + one cp.async arrival per producer lane
+      mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], 4);
     }
     sm.abort = 0;
@@ -371,29 +382,25 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
       ChainStage<MODE>& S = sm.st[st];
       const int gb = si.blk0 + lb, tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
       const size_t bh = (size_t)gb * H + h;
-      const uint32_t bytes =
-          BT * LDK * 2 + BT * LDU * 2 + 3 * BT * 4 + (MODE == CHAIN_FWD ? BT * LD64 * 2 : 0);
+      const uint32_t bytes = 2 * BT * LDK * 2 + BT * LDU * 2 + 3 * BT * 4 +
+                             (MODE == CHAIN_FWD ? BT * LDK * 2 + BT * LD64 * 2 : 0);
       if (l == 0) {
-        mbar_arrive_expect_tx(&sm.full[st], bytes);
-        bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, &sm.full[st]);
-        bulk_g2s(S.U, ws.U + (bh * NVT + tile) * BT * LDU, BT * LDU * 2, &sm.full[st]);
-        bulk_g2s(S.dec, ws.dec + bh * 3 * BT, 3 * BT * 4, &sm.full[st]);
-        if (MODE == CHAIN_FWD) bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, &sm.full[st]);
+        uint64_t* fb = &sm.full[st];
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.K, ws.Kp + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.dec, ws.dec + bh * 3 * BT, 3 * BT * 4, fb);
+        if (MODE == CHAIN_FWD) {
+          bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, BT * LDK * 2, fb);
+          bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, fb);
+        }
+        bulk_g2s(S.U, ws.U + (bh * NVT + tile) * BT * LDU, BT * LDU * 2, fb);
       }
-      // K (and Q) rows: 16-byte cp.async per lane, rows past the block's end zero-filled
-#pragma unroll 4
-      for (int idx = l; idx < BT * (DK / 8); idx += 32) {
-        const int r = idx >> 4, c = (idx & 15) * 8;
-        const bool okr = r < len;
-        const size_t off = ((size_t)(tok0 + (okr ? r : 0)) * H + h) * DK + c;
-        cp16(&S.K[r * LDK + c], k + off, okr);
-        if (MODE == CHAIN_FWD) cp16(&S.Q[r * LDK + c], q + off, okr);
-      }
-      cp_async_mbar_arrive(&sm.full[st]);
+      (void)tok0;
+      (void)len;
       ++issued;
     }
     // wait for every copy issued but not consumed (only after an abort)
-    cp_wait<0>();  // this lane's own row copies
     __syncwarp();
     if (*abort && l == 0) {
       for (int lb = max(0, issued - NS); lb < issued; ++lb) {
@@ -419,7 +426,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
               *reinterpret_cast<const uint4*>(&sm.HT[r * LDK + c]);
         }
       }
-      // X^T = H^T W^T (and H^T Q^T): even / odd k-steps accumulate separately
+      // X^T = H^T W^T (and H^T Q^T). All fragments are loaded before the MMAs
+      // so that shared-memory latency is paid once per product, not per k-step;
+      // even / odd k-steps accumulate separately.
       float x[2][2][4], o1[2][2][4];
 #pragma unroll
       for (int p = 0; p < 2; ++p)
@@ -427,18 +436,26 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) x[p][j][e] = o1[p][j][e] = 0.f;
+      {
+        uint32_t aH[DK / 16][4], bW[DK / 16][4];
 #pragma unroll
-      for (int kc = 0; kc < DK / 16; ++kc) {
-        uint32_t a[4], b[4];
-        const int p = kc & 1;
-        lda_rm(a, sm.HT, LDK, 0, 16 * kc);
-        ldb_nk_x2n(b, S.W, LDK, 16 * w, 16 * kc);
-        mma16816(x[p][0], a, b[0], b[1]);
-        mma16816(x[p][1], a, b[2], b[3]);
+        for (int kc = 0; kc < DK / 16; ++kc) {
+          lda_rm(aH[kc], sm.HT, LDK, 0, 16 * kc);
+          ldb_nk_x2n(bW[kc], S.W, LDK, 16 * w, 16 * kc);
+        }
+#pragma unroll
+        for (int kc = 0; kc < DK / 16; ++kc) {
+          mma16816(x[kc & 1][0], aH[kc], bW[kc][0], bW[kc][1]);
+          mma16816(x[kc & 1][1], aH[kc], bW[kc][2], bW[kc][3]);
+        }
         if (MODE == CHAIN_FWD) {
-          ldb_nk_x2n(b, S.Q, LDK, 16 * w, 16 * kc);
-          mma16816(o1[p][0], a, b[0], b[1]);
-          mma16816(o1[p][1], a, b[2], b[3]);
+#pragma unroll
+          for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_x2n(bW[kc], S.Q, LDK, 16 * w, 16 * kc);
+#pragma unroll
+          for (int kc = 0; kc < DK / 16; ++kc) {
+            mma16816(o1[kc & 1][0], aH[kc], bW[kc][0], bW[kc][1]);
+            mma16816(o1[kc & 1][1], aH[kc], bW[kc][2], bW[kc][3]);
+          }
         }
       }
       // V^new^T = U^T - X^T ; scaled copy for the state update
@@ -459,6 +476,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
           if (MODE == CHAIN_RECOMPUTE && ok)
             *reinterpret_cast<uint32_t*>(ws.VnT + bh * DV * BT + (size_t)(tile * 16 + vr) * BT + t0) = pv;
         }
+      // operands of the state update that do not depend on V^new: load before the barrier
+      uint32_t bK[4][8], bM[4][4];
+#pragma unroll
+      for (int kc = 0; kc < 4; ++kc) {
+        ldb_kn_x2n(&bK[kc][0], S.K, LDK, 16 * kc, 32 * w);
+        ldb_kn_x2n(&bK[kc][4], S.K, LDK, 16 * kc, 32 * w + 16);
+        if (MODE == CHAIN_FWD) ldb_nk_x2n(bM[kc], S.QKM, LD64, 16 * w, 16 * kc);
+      }
       named_bar(1, 128);
 
       // H^T <- Gamma_C H^T + Vs^T K on key columns [32w, 32w + 32)
@@ -477,22 +502,24 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) o2[p][j][e] = 0.f;
+      {
+        uint32_t aV[4][4], aN[4][4];
 #pragma unroll
-      for (int kc = 0; kc < 4; ++kc) {
-        uint32_t a[4], b[4];
-        float(*acc)[4] = (kc & 1) ? h2 : hs;
-        lda_rm(a, sm.VsT, LD64, 0, 16 * kc);
-        ldb_kn_x2n(b, S.K, LDK, 16 * kc, 32 * w);
-        mma16816(acc[0], a, b[0], b[1]);
-        mma16816(acc[1], a, b[2], b[3]);
-        ldb_kn_x2n(b, S.K, LDK, 16 * kc, 32 * w + 16);
-        mma16816(acc[2], a, b[0], b[1]);
-        mma16816(acc[3], a, b[2], b[3]);
-        if (MODE == CHAIN_FWD) {
-          lda_rm(a, sm.VnT, LD64, 0, 16 * kc);
-          ldb_nk_x2n(b, S.QKM, LD64, 16 * w, 16 * kc);
-          mma16816(o2[kc & 1][0], a, b[0], b[1]);
-          mma16816(o2[kc & 1][1], a, b[2], b[3]);
+        for (int kc = 0; kc < 4; ++kc) {
+          lda_rm(aV[kc], sm.VsT, LD64, 0, 16 * kc);
+          if (MODE == CHAIN_FWD) lda_rm(aN[kc], sm.VnT, LD64, 0, 16 * kc);
+        }
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+          float(*acc)[4] = (kc & 1) ? h2 : hs;
+          mma16816(acc[0], aV[kc], bK[kc][0], bK[kc][1]);
+          mma16816(acc[1], aV[kc], bK[kc][2], bK[kc][3]);
+          mma16816(acc[2], aV[kc], bK[kc][4], bK[kc][5]);
+          mma16816(acc[3], aV[kc], bK[kc][6], bK[kc][7]);
+          if (MODE == CHAIN_FWD) {
+            mma16816(o2[kc & 1][0], aN[kc], bM[kc][0], bM[kc][1]);
+            mma16816(o2[kc & 1][1], aN[kc], bM[kc][2], bM[kc][3]);
+          }
         }
       }
 #pragma unroll
