@@ -298,8 +298,7 @@ gdn_status run_bwd(const Plan& p, const int* cu, const void* q, const void* k, c
     if (p.varlen && (e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st)))
       return GDN_ERR_CUDA;
     const SeqMap m = make_map(p, cu, blk0, blk_seq);
-    if ((e = tc_bwd_prep(m, p.dv, q, k, v, g, beta, S_in, w, st))) return GDN_ERR_CUDA;
-    e = tc_bwd(m, p.dv, q, k, v, beta, dout, dS_out, dq, dk, dv, dg, dbeta, dS_in, w, st);
+    e = tc_bwd(m, p.dv, q, k, v, g, beta, S_in, dout, dS_out, dq, dk, dv, dg, dbeta, dS_in, w, st);
     return e ? GDN_ERR_CUDA : GDN_OK;
   }
   SimtWs w;

@@ -15,17 +15,22 @@ cudaError_t simt_bwd(const SeqMap& m, int dk, int dv, int dtype, const void* q, 
                      const void* dout, const float* dS_out, void* dq, void* dk_out, void* dv_out,
                      void* dg, void* dbeta, float* dS_in, const SimtWs& ws, cudaStream_t st);
 
-// bf16 tensor-core kernels (gdn_tc_fwd.cu, gdn_tc_bwd.cu); dk = 128, dv in {128, 256}.
+// bf16 tensor-core kernels; dk = 128, dv in {128, 256}.
+// Pre (gdn_tc_pre.cu): W, U, QKM, padded K / Q, decay factors, T.
+cudaError_t tc_pre(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const TcWs& ws, cudaStream_t st);
+// Per-block gradients (gdn_tc_grad.cu).
+cudaError_t tc_grad(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
+                    const void* beta, const void* dout, void* dq, void* dk_out, void* dv_out,
+                    void* dg, void* dbeta, const TcWs& ws, cudaStream_t st);
+// Whole forward / backward calls (gdn_tc_chain.cu).
 cudaError_t tc_fwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, void* o, float* S_out,
                    const TcWs& ws, cudaStream_t st);
-cudaError_t tc_bwd_prep(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
-                        const void* g, const void* beta, const float* S_in, const TcWs& ws,
-                        cudaStream_t st);
 cudaError_t tc_bwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
-                   const void* beta, const void* dout, const float* dS_out, void* dq, void* dk_out,
-                   void* dv_out, void* dg, void* dbeta, float* dS_in, const TcWs& ws,
-                   cudaStream_t st);
+                   const void* g, const void* beta, const float* S_in, const void* dout,
+                   const float* dS_out, void* dq, void* dk_out, void* dv_out, void* dg,
+                   void* dbeta, float* dS_in, const TcWs& ws, cudaStream_t st);
 
 // Diagnostic timing hook (include/gdn_profile.h): records an event before the
 // kernel named `next` (nullptr after the last kernel of a call) when armed.

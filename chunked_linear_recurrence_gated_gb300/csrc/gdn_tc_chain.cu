@@ -1,0 +1,688 @@
+// The sequential state chains of the bf16 tensor-core path (the ST step of the
+// StateFlow review's Pre / ST / Out decomposition, Eq. 2, and its reverse for
+// the backward pass, Eq. 6-7), plus the orchestration of the forward and
+// backward calls.
+//
+// One CTA carries RG x 16 value columns of one (sequence, head) through the
+// sequence's 64-token blocks in order: 4 compute warps and one producer warp.
+// The producer fills a ring of stages with bulk copies of the block's operand
+// tiles (written by Pre with padded rows), tracked by mbarriers; the compute
+// warps keep the fp32 state in registers and use warp-level bf16 MMAs.
+// Compute warp w owns key columns [32w, 32w + 32) of the state and tokens
+// [16w, 16w + 16) of each block.
+//
+// Forward chain, per block (H^T: value rows x key columns):
+//   X^T    = H^T W^T ;  V^new^T = U^T - X^T ;  Vs^T = V^new^T * e^{gamma_C - gamma}
+//   H^T   <- Gamma_C H^T + Vs^T K
+//   O^T    = (H^T Q^T) * Gamma + V^new^T QKM^T         (forward mode only)
+// Reverse chain, per block from the last one (dH = dS_out at the start):
+//   dV^new = QKM^T dO + Kt dH ;  dH <- Gamma_C dH + (Gamma Q)^T dO - W^T dV^new
+// The backward call runs the recompute chain (which rebuilds H_b and V^new
+// from S_in) and the reverse chain concurrently: they depend only on Pre.
+#include "gdn_internal.cuh"
+#include "gdn_mma.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int LDK = TC_LDK;
+constexpr int LD64 = TC_LD64;
+constexpr int LDU = TC_LDU;
+constexpr int DK = 128;
+constexpr int CHAIN_THREADS = 160;  // 4 compute warps + 1 producer warp
+
+enum { CHAIN_FWD = 0, CHAIN_RECOMPUTE = 1 };
+
+// ------------------------------------------------------------------ forward / recompute
+template <int MODE, int RG>
+struct FwdStage {
+  __nv_bfloat16 W[BT * LDK];
+  __nv_bfloat16 K[BT * LDK];
+  __nv_bfloat16 Q[MODE == CHAIN_FWD ? BT * LDK : 8];
+  __nv_bfloat16 QKM[MODE == CHAIN_FWD ? BT * LD64 : 8];
+  __nv_bfloat16 U[RG * BT * LDU];
+  float dec[3 * BT];
+};
+
+template <int MODE, int RG>
+constexpr int fwd_stages() {
+  return MODE == CHAIN_FWD ? 3 : 4;
+}
+
+template <int MODE, int RG>
+struct FwdSmem {
+  FwdStage<MODE, RG> st[fwd_stages<MODE, RG>()];
+  uint64_t full[fwd_stages<MODE, RG>()];
+  uint64_t empty[fwd_stages<MODE, RG>()];
+  __nv_bfloat16 HT[16 * RG * LDK];
+  __nv_bfloat16 VnT[16 * RG * LD64];
+  __nv_bfloat16 VsT[16 * RG * LD64];
+  __nv_bfloat16 O[MODE == CHAIN_FWD ? BT * (16 * RG + 8) : 8];
+  int abort;
+};
+
+template <int DV, int MODE, int RG>
+__device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
+                                               const __nv_bfloat16* __restrict__ q,
+                                               const __nv_bfloat16* __restrict__ k,
+                                               const float* S_in, float* S_out,
+                                               __nv_bfloat16* __restrict__ o, const TcWs& ws,
+                                               unsigned char* smraw) {
+  constexpr int BV = 16 * RG;
+  constexpr int NVT = DV / BV;
+  constexpr int NS = fwd_stages<MODE, RG>();
+  constexpr int LDO = BV + 8;
+  const int tile = cta % NVT;
+  const int sh = cta / NVT;
+  const int H = m.H, h = sh % H, s = sh / H;
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
+  const SeqInfo si = seq_info(m, s);
+  FwdSmem<MODE, RG>& sm = *reinterpret_cast<FwdSmem<MODE, RG>*>(smraw);
+  volatile int* abort = &sm.abort;
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], 4);
+    }
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  const size_t sbase = ((size_t)s * H + h) * DK * DV + (size_t)tile * BV;
+  // fp32 state slices: row group g holds H^T rows v = 16g + gq (+8), key columns 32w + 8j + 2tq (+1)
+  float hs[RG][4][4];
+  if (w < 4) {
+#pragma unroll
+    for (int g = 0; g < RG; ++g)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int vr = 16 * g + gq + 8 * (e >> 1);
+          const int kc = 32 * w + 8 * j + 2 * tq + (e & 1);
+          hs[g][j][e] = S_in ? S_in[sbase + (size_t)kc * DV + vr] : 0.f;
+        }
+#pragma unroll
+    for (int g = 0; g < RG; ++g)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int vr = 16 * g + gq + 8 * hf, kc = 32 * w + 8 * j + 2 * tq;
+          *reinterpret_cast<uint32_t*>(&sm.HT[vr * LDK + kc]) =
+              pack_bf16(hs[g][j][2 * hf], hs[g][j][2 * hf + 1]);
+        }
+  }
+  __syncthreads();
+
+  if (w == 4) {
+    // ---------------- producer warp
+    int issued = 0;
+    for (int lb = 0; lb < si.nblk; ++lb) {
+      const int st = lb % NS, kf = lb / NS;
+      if (lb >= NS && !mbar_wait(&sm.empty[st], (kf - 1) & 1, abort)) break;
+      FwdStage<MODE, RG>& S = sm.st[st];
+      const size_t bh = (size_t)(si.blk0 + lb) * H + h;
+      const uint32_t bytes = 2 * BT * LDK * 2 + RG * BT * LDU * 2 + 3 * BT * 4 +
+                             (MODE == CHAIN_FWD ? BT * LDK * 2 + BT * LD64 * 2 : 0);
+      if (l == 0) {
+        uint64_t* fb = &sm.full[st];
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.K, ws.Kp + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.dec, ws.dec + bh * 3 * BT, 3 * BT * 4, fb);
+        bulk_g2s(S.U, ws.U + (bh * (DV / 16) + (size_t)tile * RG) * BT * LDU, RG * BT * LDU * 2, fb);
+        if (MODE == CHAIN_FWD) {
+          bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, BT * LDK * 2, fb);
+          bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, fb);
+        }
+      }
+      ++issued;
+    }
+    __syncwarp();
+    if (*abort && l == 0) {  // after a timeout: let every copy still in flight land
+      for (int lb = max(0, issued - NS); lb < issued; ++lb) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&sm.full[lb % NS], (lb / NS) & 1) && clock64() - t0 < (1ll << 31)) {
+        }
+      }
+    }
+  } else {
+    // ---------------- compute warps
+    for (int lb = 0; lb < si.nblk; ++lb) {
+      const int st = lb % NS;
+      const bool ok = mbar_wait(&sm.full[st], (lb / NS) & 1, abort);
+      const FwdStage<MODE, RG>& S = sm.st[st];
+      const int tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
+      const size_t bh = (size_t)(si.blk0 + lb) * H + h;
+      const float* dec = S.dec;
+      if (MODE == CHAIN_RECOMPUTE && ok) {
+        __nv_bfloat16* Hg = ws.HbT + bh * DV * DK + (size_t)tile * BV * DK;
+        for (int idx = tid; idx < BV * 16; idx += 128) {
+          const int r = idx >> 4, c = (idx & 15) * 8;
+          *reinterpret_cast<uint4*>(Hg + r * DK + c) =
+              *reinterpret_cast<const uint4*>(&sm.HT[r * LDK + c]);
+        }
+      }
+      // X^T = H^T W^T (and H^T Q^T); W / Q fragments are shared by the row groups
+      float x[RG][2][2][4], o1[RG][2][2][4];
+#pragma unroll
+      for (int g = 0; g < RG; ++g)
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[g][p][j][e] = o1[g][p][j][e] = 0.f;
+      {
+        uint32_t bW[DK / 16][4];
+#pragma unroll
+        for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_x2n(bW[kc], S.W, LDK, 16 * w, 16 * kc);
+#pragma unroll
+        for (int g = 0; g < RG; ++g) {
+          uint32_t aH[DK / 16][4];
+#pragma unroll
+          for (int kc = 0; kc < DK / 16; ++kc) lda_rm(aH[kc], sm.HT, LDK, 16 * g, 16 * kc);
+#pragma unroll
+          for (int kc = 0; kc < DK / 16; ++kc) {
+            mma16816(x[g][kc & 1][0], aH[kc], bW[kc][0], bW[kc][1]);
+            mma16816(x[g][kc & 1][1], aH[kc], bW[kc][2], bW[kc][3]);
+          }
+        }
+        if (MODE == CHAIN_FWD) {
+#pragma unroll
+          for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_x2n(bW[kc], S.Q, LDK, 16 * w, 16 * kc);
+#pragma unroll
+          for (int g = 0; g < RG; ++g) {
+            uint32_t aH[DK / 16][4];
+#pragma unroll
+            for (int kc = 0; kc < DK / 16; ++kc) lda_rm(aH[kc], sm.HT, LDK, 16 * g, 16 * kc);
+#pragma unroll
+            for (int kc = 0; kc < DK / 16; ++kc) {
+              mma16816(o1[g][kc & 1][0], aH[kc], bW[kc][0], bW[kc][1]);
+              mma16816(o1[g][kc & 1][1], aH[kc], bW[kc][2], bW[kc][3]);
+            }
+          }
+        }
+      }
+      // V^new^T = U^T - X^T ; scaled copy for the state update
+#pragma unroll
+      for (int g = 0; g < RG; ++g)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int vr = 16 * g + gq + 8 * hf;
+            const int t0 = 16 * w + 8 * j + 2 * tq;
+            const __nv_bfloat16* Ug = S.U + g * BT * LDU;
+            const float u0 = __bfloat162float(Ug[t0 * LDU + gq + 8 * hf]);
+            const float u1 = __bfloat162float(Ug[(t0 + 1) * LDU + gq + 8 * hf]);
+            const float v0 = u0 - (x[g][0][j][2 * hf] + x[g][1][j][2 * hf]);
+            const float v1 = u1 - (x[g][0][j][2 * hf + 1] + x[g][1][j][2 * hf + 1]);
+            const uint32_t pv = pack_bf16(v0, v1);
+            *reinterpret_cast<uint32_t*>(&sm.VnT[vr * LD64 + t0]) = pv;
+            *reinterpret_cast<uint32_t*>(&sm.VsT[vr * LD64 + t0]) =
+                pack_bf16(v0 * dec[BT + t0], v1 * dec[BT + t0 + 1]);
+            if (MODE == CHAIN_RECOMPUTE && ok)
+              *reinterpret_cast<uint32_t*>(ws.VnT + bh * DV * BT + (size_t)(tile * BV + vr) * BT + t0) = pv;
+          }
+      // operands of the state update that do not depend on V^new: load before the barrier
+      uint32_t bK[4][8], bM[4][4];
+#pragma unroll
+      for (int kc = 0; kc < 4; ++kc) {
+        ldb_kn_x2n(&bK[kc][0], S.K, LDK, 16 * kc, 32 * w);
+        ldb_kn_x2n(&bK[kc][4], S.K, LDK, 16 * kc, 32 * w + 16);
+        if (MODE == CHAIN_FWD) ldb_nk_x2n(bM[kc], S.QKM, LD64, 16 * w, 16 * kc);
+      }
+      named_bar(1, 128);
+
+      // H^T <- Gamma_C H^T + Vs^T K on key columns [32w, 32w + 32)
+      const float GC = dec[BT - 1];
+      float o2[RG][2][4];
+#pragma unroll
+      for (int g = 0; g < RG; ++g) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o2[g][j][e] = 0.f;
+        float h2[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hs[g][j][e] *= GC;
+            h2[j][e] = 0.f;
+          }
+        uint32_t aV[4][4];
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) lda_rm(aV[kc], sm.VsT, LD64, 16 * g, 16 * kc);
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+          float(*acc)[4] = (kc & 1) ? h2 : hs[g];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma16816(acc[j], aV[kc], bK[kc][2 * j], bK[kc][2 * j + 1]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) hs[g][j][e] += h2[j][e];
+        if (MODE == CHAIN_FWD) {
+#pragma unroll
+          for (int kc = 0; kc < 4; ++kc) lda_rm(aV[kc], sm.VnT, LD64, 16 * g, 16 * kc);
+#pragma unroll
+          for (int kc = 0; kc < 4; ++kc) {
+            mma16816(o2[g][0], aV[kc], bM[kc][0], bM[kc][1]);
+            mma16816(o2[g][1], aV[kc], bM[kc][2], bM[kc][3]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int vr = 16 * g + gq + 8 * hf, kc = 32 * w + 8 * j + 2 * tq;
+            *reinterpret_cast<uint32_t*>(&sm.HT[vr * LDK + kc]) =
+                pack_bf16(hs[g][j][2 * hf], hs[g][j][2 * hf + 1]);
+          }
+      }
+      if (MODE == CHAIN_FWD) {
+        // O[token][v] = Gamma_token (H^T Q^T)^T + (V^new^T QKM^T)^T, staged for coalesced stores
+#pragma unroll
+        for (int g = 0; g < RG; ++g)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int vr = 16 * g + gq + 8 * (e >> 1);
+              const int t = 16 * w + 8 * j + 2 * tq + (e & 1);
+              sm.O[t * LDO + vr] = __float2bfloat16_rn(
+                  dec[t] * (o1[g][0][j][e] + o1[g][1][j][e]) + o2[g][j][e]);
+            }
+        __syncwarp();
+        // each warp stores its own 16 tokens: BV / 8 chunks of 16 bytes per row
+        for (int idx = l; idx < 16 * (BV / 8); idx += 32) {
+          const int r = 16 * w + idx / (BV / 8), c = (idx % (BV / 8)) * 8;
+          if (r < len && ok)
+            *reinterpret_cast<uint4*>(o + ((size_t)(tok0 + r) * H + h) * DV + tile * BV + c) =
+                *reinterpret_cast<const uint4*>(&sm.O[r * LDO + c]);
+        }
+      }
+      __syncwarp();
+      if (l == 0) mbar_arrive(&sm.empty[st]);
+      named_bar(1, 128);
+    }
+    if (S_out && !*abort) {
+#pragma unroll
+      for (int g = 0; g < RG; ++g)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int vr = 16 * g + gq + 8 * (e >> 1);
+            const int kc = 32 * w + 8 * j + 2 * tq + (e & 1);
+            S_out[sbase + (size_t)kc * DV + vr] = hs[g][j][e];
+          }
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && *abort) ws.status[0] = DEV_TIMEOUT;
+}
+
+// ------------------------------------------------------------------ reverse chain
+template <int RG>
+struct RevStage {
+  __nv_bfloat16 W[BT * LDK];
+  __nv_bfloat16 K[BT * LDK];
+  __nv_bfloat16 Q[BT * LDK];
+  __nv_bfloat16 QKM[BT * LD64];
+  __nv_bfloat16 dO[BT * (16 * RG + 8)];
+  float dec[3 * BT];
+};
+
+constexpr int REV_STAGES = 3;
+
+template <int RG>
+struct RevSmem {
+  RevStage<RG> st[REV_STAGES];
+  uint64_t full[REV_STAGES];
+  uint64_t empty[REV_STAGES];
+  __nv_bfloat16 dHT[16 * RG * LDK];   // bf16 copy of dH^T (value rows)
+  __nv_bfloat16 dVT[16 * RG * LD64];  // -dV^new^T (value rows)
+  __nv_bfloat16 dOs[BT * (16 * RG + 8)];  // diag(Gamma) dO tile
+  int abort;
+};
+
+template <int DV, int RG>
+__device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
+                                               const __nv_bfloat16* __restrict__ q,
+                                               const __nv_bfloat16* __restrict__ k,
+                                               const __nv_bfloat16* __restrict__ dout,
+                                               const float* dS_out, float* dS_in, const TcWs& ws,
+                                               unsigned char* smraw) {
+  constexpr int BV = 16 * RG;
+  constexpr int NVT = DV / BV;
+  constexpr int NS = REV_STAGES;
+  constexpr int LDO = BV + 8;
+  const int tile = cta % NVT;
+  const int sh = cta / NVT;
+  const int H = m.H, h = sh % H, s = sh / H;
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
+  const SeqInfo si = seq_info(m, s);
+  RevSmem<RG>& sm = *reinterpret_cast<RevSmem<RG>*>(smraw);
+  volatile int* abort = &sm.abort;
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&sm.full[i], 1 + 32);  // bulk-copy arrival + one cp.async arrival per producer lane
+      mbar_init(&sm.empty[i], 4);
+    }
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  float dh[RG][4][4];
+  const size_t sbase = ((size_t)s * H + h) * DK * DV + (size_t)tile * BV;
+  if (w < 4) {
+#pragma unroll
+    for (int g = 0; g < RG; ++g)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int vr = 16 * g + gq + 8 * (e >> 1);
+          const int kc = 32 * w + 8 * j + 2 * tq + (e & 1);
+          dh[g][j][e] = dS_out ? dS_out[sbase + (size_t)kc * DV + vr] : 0.f;
+        }
+#pragma unroll
+    for (int g = 0; g < RG; ++g)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int vr = 16 * g + gq + 8 * hf, kc = 32 * w + 8 * j + 2 * tq;
+          *reinterpret_cast<uint32_t*>(&sm.dHT[vr * LDK + kc]) =
+              pack_bf16(dh[g][j][2 * hf], dh[g][j][2 * hf + 1]);
+        }
+  }
+  __syncthreads();
+
+  if (w == 4) {
+    // ---------------- producer warp: iteration it loads block nblk - 1 - it
+    int issued = 0;
+    for (int it = 0; it < si.nblk; ++it) {
+      const int st = it % NS, kf = it / NS;
+      if (it >= NS && !mbar_wait(&sm.empty[st], (kf - 1) & 1, abort)) break;
+      RevStage<RG>& S = sm.st[st];
+      const int lb = si.nblk - 1 - it;
+      const int tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
+      const size_t bh = (size_t)(si.blk0 + lb) * H + h;
+      const uint32_t bytes = 3 * BT * LDK * 2 + BT * LD64 * 2 + 3 * BT * 4;
+      if (l == 0) {
+        uint64_t* fb = &sm.full[st];
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.K, ws.Kp + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, fb);
+        bulk_g2s(S.dec, ws.dec + bh * 3 * BT, 3 * BT * 4, fb);
+      }
+      // the dO tile: 16-byte cp.async per lane, rows past the block's end zero-filled
+#pragma unroll
+      for (int idx = l; idx < BT * (BV / 8); idx += 32) {
+        const int r = idx / (BV / 8), c = (idx % (BV / 8)) * 8;
+        const bool okr = r < len;
+        const size_t tok = (size_t)(tok0 + (okr ? r : 0)) * H + h;
+        cp16(&S.dO[r * LDO + c], dout + tok * DV + tile * BV + c, okr);
+      }
+      cp_async_mbar_arrive(&sm.full[st]);
+      ++issued;
+    }
+    cp_wait<0>();
+    __syncwarp();
+    if (*abort && l == 0) {
+      for (int it = max(0, issued - NS); it < issued; ++it) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&sm.full[it % NS], (it / NS) & 1) && clock64() - t0 < (1ll << 31)) {
+        }
+      }
+    }
+  } else {
+    // ---------------- compute warps
+    for (int it = 0; it < si.nblk; ++it) {
+      const int st = it % NS;
+      const bool ok = mbar_wait(&sm.full[st], (it / NS) & 1, abort);
+      const RevStage<RG>& S = sm.st[st];
+      const int lb = si.nblk - 1 - it;
+      const size_t bh = (size_t)(si.blk0 + lb) * H + h;
+      const float* dec = S.dec;
+      // dH_{b+1} (bf16, value-major) for the gradient kernel
+      if (ok) {
+        __nv_bfloat16* Dg = ws.dHT + bh * DV * DK + (size_t)tile * BV * DK;
+        for (int idx = tid; idx < BV * 16; idx += 128) {
+          const int r = idx >> 4, c = (idx & 15) * 8;
+          *reinterpret_cast<uint4*>(Dg + r * DK + c) =
+              *reinterpret_cast<const uint4*>(&sm.dHT[r * LDK + c]);
+        }
+      }
+      // diag(Gamma) dO for the off-chain term (warp w: rows 16w..16w+15)
+      for (int idx = l; idx < 16 * (BV / 8); idx += 32) {
+        const int r = 16 * w + idx / (BV / 8), c = (idx % (BV / 8)) * 8;
+        const float G = dec[r];
+        const uint4 raw = *reinterpret_cast<const uint4*>(&S.dO[r * LDO + c]);
+        const uint32_t* pr = reinterpret_cast<const uint32_t*>(&raw);
+        uint4 outv;
+        uint32_t* po = reinterpret_cast<uint32_t*>(&outv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack_bf16(pr[e]);
+          po[e] = pack_bf16(G * f.x, G * f.y);
+        }
+        *reinterpret_cast<uint4*>(&sm.dOs[r * LDO + c]) = outv;
+      }
+      // dV^new^T for tokens [16w, 16w + 16): dO^T QKM + (dH^T K^T) * e^{gamma_C - gamma}
+      {
+        uint32_t bK[DK / 16][4], bM[4][4];
+#pragma unroll
+        for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_x2n(bK[kc], S.K, LDK, 16 * w, 16 * kc);
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) ldb_kn_x2n(bM[kc], S.QKM, LD64, 16 * kc, 16 * w);
+#pragma unroll
+        for (int g = 0; g < RG; ++g) {
+          float a1[2][4], a2[2][2][4];
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a1[j][e] = a2[0][j][e] = a2[1][j][e] = 0.f;
+          uint32_t aD[DK / 16][4];
+#pragma unroll
+          for (int kc = 0; kc < DK / 16; ++kc) lda_rm(aD[kc], sm.dHT, LDK, 16 * g, 16 * kc);
+#pragma unroll
+          for (int kc = 0; kc < DK / 16; ++kc) {
+            mma16816(a2[kc & 1][0], aD[kc], bK[kc][0], bK[kc][1]);
+            mma16816(a2[kc & 1][1], aD[kc], bK[kc][2], bK[kc][3]);
+          }
+#pragma unroll
+          for (int kc = 0; kc < 4; ++kc) lda_tr(aD[kc], S.dO, LDO, 16 * g, 16 * kc);
+#pragma unroll
+          for (int kc = 0; kc < 4; ++kc) {
+            mma16816(a1[0], aD[kc], bM[kc][0], bM[kc][1]);
+            mma16816(a1[1], aD[kc], bM[kc][2], bM[kc][3]);
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int vr = 16 * g + gq + 8 * hf;
+              const int t0 = 16 * w + 8 * j + 2 * tq;
+              const float d0 = a1[j][2 * hf] + dec[BT + t0] * (a2[0][j][2 * hf] + a2[1][j][2 * hf]);
+              const float d1 =
+                  a1[j][2 * hf + 1] + dec[BT + t0 + 1] * (a2[0][j][2 * hf + 1] + a2[1][j][2 * hf + 1]);
+              *reinterpret_cast<uint32_t*>(&sm.dVT[vr * LD64 + t0]) = pack_bf16(-d0, -d1);
+              if (ok)
+                *reinterpret_cast<uint32_t*>(ws.dVnT + bh * DV * BT + (size_t)(tile * BV + vr) * BT + t0) =
+                    pack_bf16(d0, d1);
+            }
+        }
+      }
+      // operands that do not depend on dV^new: load before the barrier
+      uint32_t bQ[4][8], bW[4][8];
+#pragma unroll
+      for (int kc = 0; kc < 4; ++kc) {
+        ldb_kn_x2n(&bQ[kc][0], S.Q, LDK, 16 * kc, 32 * w);
+        ldb_kn_x2n(&bQ[kc][4], S.Q, LDK, 16 * kc, 32 * w + 16);
+        ldb_kn_x2n(&bW[kc][0], S.W, LDK, 16 * kc, 32 * w);
+        ldb_kn_x2n(&bW[kc][4], S.W, LDK, 16 * kc, 32 * w + 16);
+      }
+      named_bar(1, 128);
+      // dH^T <- Gamma_C dH^T + (Gamma dO)^T Q - dV^new^T W on key columns [32w, 32w + 32)
+      const float GC = dec[BT - 1];
+#pragma unroll
+      for (int g = 0; g < RG; ++g) {
+        float d2[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dh[g][j][e] *= GC;
+            d2[j][e] = 0.f;
+          }
+        uint32_t aO[4][4], aV[4][4];
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+          lda_tr(aO[kc], sm.dOs, LDO, 16 * g, 16 * kc);
+          lda_rm(aV[kc], sm.dVT, LD64, 16 * g, 16 * kc);
+        }
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma16816(dh[g][j], aO[kc], bQ[kc][2 * j], bQ[kc][2 * j + 1]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma16816(d2[j], aV[kc], bW[kc][2 * j], bW[kc][2 * j + 1]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dh[g][j][e] += d2[j][e];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int vr = 16 * g + gq + 8 * hf, kc = 32 * w + 8 * j + 2 * tq;
+            *reinterpret_cast<uint32_t*>(&sm.dHT[vr * LDK + kc]) =
+                pack_bf16(dh[g][j][2 * hf], dh[g][j][2 * hf + 1]);
+          }
+      }
+      __syncwarp();
+      if (l == 0) mbar_arrive(&sm.empty[st]);
+      named_bar(1, 128);
+    }
+    if (dS_in && !*abort) {
+#pragma unroll
+      for (int g = 0; g < RG; ++g)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int vr = 16 * g + gq + 8 * (e >> 1);
+            const int kc = 32 * w + 8 * j + 2 * tq + (e & 1);
+            dS_in[sbase + (size_t)kc * DV + vr] = dh[g][j][e];
+          }
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && *abort) ws.status[0] = DEV_TIMEOUT;
+}
+
+// ------------------------------------------------------------------ kernels
+// Forward: 16 value columns per CTA (the most SMs per head: the chain step is
+// bounded by each CTA's shared-memory traffic, which does not shrink with fewer
+// columns per CTA).
+template <int DV>
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+    k_chain_fwd(SeqMap m, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                const float* S_in, float* S_out, __nv_bfloat16* __restrict__ o, TcWs ws) {
+  extern __shared__ __align__(128) unsigned char smraw[];
+  if (m.cu == nullptr && blockIdx.x == 0 && threadIdx.x == 0) ws.status[0] = DEV_OK;
+  chain_fwd_body<DV, CHAIN_FWD, 1>(m, blockIdx.x, q, k, S_in, S_out, o, ws, smraw);
+}
+
+// Backward: the recompute chain (CTAs [0, n)) and the reverse chain (CTAs
+// [n, 2n)) run side by side, 32 value columns per CTA.
+constexpr int BWD_RG = 2;
+
+template <int DV>
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+    k_chains_bwd(SeqMap m, int n, const __nv_bfloat16* __restrict__ q,
+                 const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ dout,
+                 const float* S_in, const float* dS_out, float* dS_in, TcWs ws) {
+  extern __shared__ __align__(128) unsigned char smraw[];
+  if (m.cu == nullptr && blockIdx.x == 0 && threadIdx.x == 0) ws.status[0] = DEV_OK;
+  if ((int)blockIdx.x < n)
+    chain_fwd_body<DV, CHAIN_RECOMPUTE, BWD_RG>(m, blockIdx.x, q, k, S_in, nullptr, nullptr, ws,
+                                               smraw);
+  else
+    chain_rev_body<DV, BWD_RG>(m, blockIdx.x - n, q, k, dout, dS_out, dS_in, ws, smraw);
+}
+
+template <class K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int DV>
+cudaError_t fwd_t(const SeqMap& m, const void* q, const void* k, const void* v, const void* g,
+                  const void* beta, const float* S_in, void* o, float* S_out, const TcWs& ws,
+                  cudaStream_t st) {
+  using bf = __nv_bfloat16;
+  cudaError_t e;
+  if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, st))) return e;
+  constexpr size_t smem = sizeof(FwdSmem<CHAIN_FWD, 1>);
+  if ((e = set_smem(k_chain_fwd<DV>, smem))) return e;
+  prof_mark(st, "tc_chain_fwd");
+  k_chain_fwd<DV><<<m.nseq * m.H * (DV / 16), CHAIN_THREADS, smem, st>>>(
+      m, (const bf*)q, (const bf*)k, S_in, S_out, (bf*)o, ws);
+  prof_mark(st, nullptr);
+  return cudaGetLastError();
+}
+
+template <int DV>
+cudaError_t bwd_t(const SeqMap& m, const void* q, const void* k, const void* v, const void* g,
+                  const void* beta, const float* S_in, const void* dout, const float* dS_out,
+                  void* dq, void* dkk, void* dvv, void* dg, void* dbeta, float* dS_in,
+                  const TcWs& ws, cudaStream_t st) {
+  using bf = __nv_bfloat16;
+  cudaError_t e;
+  if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, st))) return e;
+  constexpr size_t s1 = sizeof(FwdSmem<CHAIN_RECOMPUTE, BWD_RG>);
+  constexpr size_t s2 = sizeof(RevSmem<BWD_RG>);
+  constexpr size_t smem = s1 > s2 ? s1 : s2;
+  if ((e = set_smem(k_chains_bwd<DV>, smem))) return e;
+  const int n = m.nseq * m.H * (DV / (16 * BWD_RG));
+  prof_mark(st, "tc_chains_bwd");
+  k_chains_bwd<DV><<<2 * n, CHAIN_THREADS, smem, st>>>(m, n, (const bf*)q, (const bf*)k,
+                                                     (const bf*)dout, S_in, dS_out, dS_in, ws);
+  if ((e = cudaGetLastError())) return e;
+  if ((e = tc_grad(m, DV, q, k, v, beta, dout, dq, dkk, dvv, dg, dbeta, ws, st))) return e;
+  prof_mark(st, nullptr);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_fwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const float* S_in, void* o, float* S_out,
+                   const TcWs& ws, cudaStream_t st) {
+  if (dv == 128) return fwd_t<128>(m, q, k, v, g, beta, S_in, o, S_out, ws, st);
+  return fwd_t<256>(m, q, k, v, g, beta, S_in, o, S_out, ws, st);
+}
+
+cudaError_t tc_bwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const float* S_in, const void* dout,
+                   const float* dS_out, void* dq, void* dkk, void* dvv, void* dg, void* dbeta,
+                   float* dS_in, const TcWs& ws, cudaStream_t st) {
+  if (dv == 128)
+    return bwd_t<128>(m, q, k, v, g, beta, S_in, dout, dS_out, dq, dkk, dvv, dg, dbeta, dS_in, ws,
+                      st);
+  return bwd_t<256>(m, q, k, v, g, beta, S_in, dout, dS_out, dq, dkk, dvv, dg, dbeta, dS_in, ws,
+                    st);
+}
+
+}  // namespace gdn
