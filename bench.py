@@ -210,6 +210,18 @@ def barrier(world):
         torch.distributed.barrier()
 
 
+def aggregate(ms_step_local, tokens_per_rank, world, device=None):
+    """Whole-job throughput of a weak-scaling run: every rank processed its own
+    `tokens_per_rank` tokens; the step time is the slowest rank's (max over
+    ranks). Returns (ms_per_step, tokens_per_second)."""
+    ms = float(ms_step_local)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, tokens_per_rank * world / (ms / 1e3)
+
+
 def time_steps(fn, K, dev):
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
@@ -353,13 +365,8 @@ def main():
     with ClockSampler(local) as clk:
         ms = time_steps(runner.step, args.steps, dev)
     barrier(world)
-    ms_step = ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step, value = aggregate(ms / args.steps, w.B * w.T, world, device=dev)
     tokens = w.B * w.T * world
-    value = tokens / (ms_step / 1e3)
 
     # per-kernel timing on the launch stream (instrumented replay of the same steps)
     timer = gdn.KernelTimer(capacity=4096)

@@ -177,8 +177,10 @@ size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, c
   const size_t o_Kp = c.take(2 * nbh * BT * TC_LDK);
   const size_t o_Qp = c.take(2 * nbh * BT * TC_LDK);
   size_t o_T = 0, o_Hb = 0, o_Vn = 0, o_dH = 0, o_dVn = 0;
+  size_t o_KKM = 0;
   if (bwd) {
     o_T = c.take(2 * nbh * BT * BT);
+    o_KKM = c.take(2 * nbh * BT * TC_LD64);
     o_Hb = c.take(2 * nbh * p.dv * p.dk);
     o_Vn = c.take(2 * nbh * p.dv * BT);
     o_dH = c.take(2 * nbh * p.dv * p.dk);
@@ -194,6 +196,7 @@ size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, c
     ws->Kp = (bf*)(base + o_Kp);
     ws->Qp = (bf*)(base + o_Qp);
     ws->T = bwd ? (bf*)(base + o_T) : nullptr;
+    ws->KKM = bwd ? (bf*)(base + o_KKM) : nullptr;
     ws->HbT = bwd ? (bf*)(base + o_Hb) : nullptr;
     ws->VnT = bwd ? (bf*)(base + o_Vn) : nullptr;
     ws->dHT = bwd ? (bf*)(base + o_dH) : nullptr;

@@ -98,6 +98,7 @@ struct TcWs {
   __nv_bfloat16* Kp;     // [nblk, H, BT, TC_LDK]          K rows (padded copy, zero past the end)
   __nv_bfloat16* Qp;     // [nblk, H, BT, TC_LDK]          Q rows (padded copy, zero past the end)
   __nv_bfloat16* T;      // [nblk, H, BT, BT]      (I + A)^-1          (backward)
+  __nv_bfloat16* KKM;    // [nblk, H, BT, TC_LD64] K K^T * Mask, strictly lower (backward)
   __nv_bfloat16* HbT;    // [nblk, H, dv, 128]     H_b^T               (backward)
   __nv_bfloat16* VnT;    // [nblk, H, dv, BT]      V^new^T             (backward)
   __nv_bfloat16* dHT;    // [nblk, H, dv, 128]     dH_{b+1}^T          (backward)

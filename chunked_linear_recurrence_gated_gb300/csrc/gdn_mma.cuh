@@ -222,3 +222,24 @@ __device__ __forceinline__ void bulk_g2s_mc(void* dst, const void* src, uint32_t
       : "memory");
 }
 }  // namespace gdn
+
+namespace gdn {
+// ---------------------------------------------------------------- TF32 warp-level MMA
+// mma.m16n8k8 with tf32 inputs (fp32 storage, 10-bit mantissa) and fp32
+// accumulation. Fragments (g = lane / 4, t = lane % 4):
+//   A (16 x 8): a0 (g, t) a1 (g+8, t) a2 (g, t+4) a3 (g+8, t+4)
+//   B (8 x 8):  b0 (k t, n g) b1 (k t+4, n g)
+//   C (16 x 8): c0, c1 (g, 2t..2t+1) c2, c3 (g+8, 2t..2t+1)
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+}  // namespace gdn

@@ -284,56 +284,35 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
         *reinterpret_cast<uint32_t*>(&sm.u.late.HW[r * LDK + c]) = pack_bf16(aHW[j][2 * hf], aHW[j][2 * hf + 1]);
       }
   }
-  // ---- P = dOV * Mask -> smem ; partial dT = beta_c dWV
-  float dT[4][4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = R0 + gq + 8 * (e >> 1), c = 32 * cw + 8 * j + 2 * tq + (e & 1);
-      const float msk = (c <= r) ? __expf(sm.g[r] - sm.g[c]) : 0.f;
-      sm.u.late.P[r * LD64 + c] = __float2bfloat16_rn(aOV[j][e] * msk);
-      aOV[j][e] *= msk;  // P in fp32
-      dT[j][e] = sm.b[c] * aWV[j][e];
-    }
-  __syncthreads();
-  // ---- QK, KK, HW K^T on this warp's 64 x 64 tile
-  float qk[4][4], kk[4][4], hk[4][4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) qk[j][e] = kk[j][e] = hk[j][e] = 0.f;
-#pragma unroll
-  for (int kc = 0; kc < DK / 16; ++kc) {
-    uint32_t aq_[4], ak_[4], ah_[4];
-    lda_rm(aq_, sm.Q, LDK, R0, 16 * kc);
-    lda_rm(ak_, sm.K, LDK, R0, 16 * kc);
-    lda_rm(ah_, sm.u.late.HW, LDK, R0, 16 * kc);
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-      uint32_t b[4];
-      ldb_nk_x2n(b, sm.K, LDK, 32 * cw + 16 * jj, 16 * kc);
-      mma16816(qk[2 * jj], aq_, b[0], b[1]);
-      mma16816(qk[2 * jj + 1], aq_, b[2], b[3]);
-      mma16816(kk[2 * jj], ak_, b[0], b[1]);
-      mma16816(kk[2 * jj + 1], ak_, b[2], b[3]);
-      mma16816(hk[2 * jj], ah_, b[0], b[1]);
-      mma16816(hk[2 * jj + 1], ah_, b[2], b[3]);
-    }
-  }
-  // R = P * QK -> row / column sums ; dT = beta_c dWV - beta_c Gamma_c (HW K^T)
+  // ---- P = dOV * Mask -> smem ; R = P * (Q K^T) = dOV * QKM (Pre's masked Q K^T)
+  //      -> row / column sums ; partial dT = beta_c dWV ; K K^T * Mask for the dA step
+  float dT[4][4], kk[4][4];
   {
+    const __nv_bfloat16* qkm = ws.QKM + bh * BT * LD64;
+    const __nv_bfloat16* kkm = ws.KKM + bh * BT * LD64;
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float cs0 = 0.f, cs1 = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c = 32 * cw + 8 * j + 2 * tq + (e & 1);
-        const float R = aOV[j][e] * qk[j][e];
-        if (e < 2) rs0 += R; else rs1 += R;
-        if (e & 1) cs1 += R; else cs0 += R;
-        dT[j][e] -= sm.b[c] * sm.G[c] * hk[j][e];
+      for (int hf = 0; hf < 2; ++hf) {
+        const int r = R0 + gq + 8 * hf, c = 32 * cw + 8 * j + 2 * tq;
+        const float2 qm = unpack_bf16(*reinterpret_cast<const uint32_t*>(qkm + r * LD64 + c));
+        const float2 km = unpack_bf16(*reinterpret_cast<const uint32_t*>(kkm + r * LD64 + c));
+        kk[j][2 * hf] = km.x;
+        kk[j][2 * hf + 1] = km.y;
+        const float m0 = (c <= r) ? __expf(sm.g[r] - sm.g[c]) : 0.f;
+        const float m1 = (c + 1 <= r) ? __expf(sm.g[r] - sm.g[c + 1]) : 0.f;
+        const float R0v = aOV[j][2 * hf] * qm.x, R1v = aOV[j][2 * hf + 1] * qm.y;
+        if (hf == 0) rs0 += R0v + R1v; else rs1 += R0v + R1v;
+        cs0 += R0v;
+        cs1 += R1v;
+        aOV[j][2 * hf] *= m0;  // P in fp32
+        aOV[j][2 * hf + 1] *= m1;
+        *reinterpret_cast<uint32_t*>(&sm.u.late.P[r * LD64 + c]) =
+            pack_bf16(aOV[j][2 * hf], aOV[j][2 * hf + 1]);
+        dT[j][2 * hf] = sm.b[c] * aWV[j][2 * hf];
+        dT[j][2 * hf + 1] = sm.b[c + 1] * aWV[j][2 * hf + 1];
       }
       cs0 = col_reduce(cs0);
       cs1 = col_reduce(cs1);
@@ -349,6 +328,33 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       sm.rowacc[cw][R0 + gq] += rs0;
       sm.rowacc[cw][R0 + gq + 8] += rs1;
     }
+  }
+  __syncthreads();
+  // ---- dT = beta_c dWV - beta_c Gamma_c (HW K^T) on this warp's 64 x 64 tile
+  {
+    float hk[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) hk[j][e] = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < DK / 16; ++kc) {
+      uint32_t ah_[4], b0[4], b1[4];
+      lda_rm(ah_, sm.u.late.HW, LDK, R0, 16 * kc);
+      ldb_nk_x2n(b0, sm.K, LDK, 32 * cw, 16 * kc);
+      ldb_nk_x2n(b1, sm.K, LDK, 32 * cw + 16, 16 * kc);
+      mma16816(hk[0], ah_, b0[0], b0[1]);
+      mma16816(hk[1], ah_, b0[2], b0[3]);
+      mma16816(hk[2], ah_, b1[0], b1[1]);
+      mma16816(hk[3], ah_, b1[2], b1[3]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 32 * cw + 8 * j + 2 * tq + (e & 1);
+        dT[j][e] -= sm.b[c] * sm.G[c] * hk[j][e];
+      }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -458,12 +464,13 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
         const int r = R0 + gq + 8 * (e >> 1), c = 32 * cw + 8 * j + 2 * tq + (e & 1);
         const float dA = (c < r) ? -da[j][e] : 0.f;
         const float E = (c < r) ? dA * __expf(sm.g[r] - sm.g[c]) : 0.f;
-        const float Gv = sm.b[r] * E * kk[j][e];
+        const float dAK = dA * kk[j][e];  // dA * K K^T * Mask = E * K K^T
+        const float Gv = sm.b[r] * dAK;
         if (e < 2) {
-          pb0 += E * kk[j][e];
+          pb0 += dAK;
           rg0 += Gv;
         } else {
-          pb1 += E * kk[j][e];
+          pb1 += dAK;
           rg1 += Gv;
         }
         if (e & 1) cg1 += Gv; else cg0 += Gv;

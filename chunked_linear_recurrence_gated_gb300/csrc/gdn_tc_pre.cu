@@ -28,7 +28,7 @@ struct PreSmem {
   __nv_bfloat16 Q[BT * LDK];  // reused as the fp32 strictly-lower A (same size) after Q K^T
   __nv_bfloat16 V[BT * (DV + 8)];
   float Tf[BT * 68];          // T (fp32)
-  float S[3 * 16 * 17];       // block products of the inverse
+  float S[16 * 52];           // block-row product of the inverse
   __nv_bfloat16 Tw[BT * LD64];  // T diag(beta Gamma)
   __nv_bfloat16 Tu[BT * LD64];  // T diag(beta)
   float g[BT];
@@ -58,11 +58,14 @@ __device__ __forceinline__ void block_cumsum64(float* sg) {
 }
 
 // T = (I + A)^-1 for strictly-lower 64 x 64 A (fp32, ld 68), NT threads.
-// Diagonal 16 x 16 blocks by forward substitution (one warp each), then block
-// rows i = 1..3: T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj.
+// The four diagonal 16 x 16 blocks by fp32 forward substitution (one warp
+// each); then, block row by block row (i = 1..3), warp 0 forms
+//   S = A[i, 0:i] T[0:i, 0:i]   and   T[i, 0:i] = -T_ii S
+// with TF32 tensor-core MMAs (fp32 accumulation): the block products of
+// T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj for all j < i at once.
 template <int NT>
 __device__ void invert_unit_lower64(const float* A, float* Tf, float* S) {
-  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, g = l >> 2, t = l & 3;
   for (int idx = tid; idx < BT * 68; idx += NT) Tf[idx] = 0.f;
   __syncthreads();
   if (w < 4 && l < 16) {
@@ -79,29 +82,52 @@ __device__ void invert_unit_lower64(const float* A, float* Tf, float* S) {
     }
   }
   __syncthreads();
-  for (int i = 1; i < 4; ++i) {
-    for (int idx = tid; idx < i * 256; idx += NT) {
-      const int j = idx >> 8, e = idx & 255, r = e >> 4, c = e & 15;
-      float acc = 0.f;
-      for (int m = j; m < i; ++m) {
-        const float* Ar = A + (16 * i + r) * 68 + 16 * m;
-        const float* Tc = Tf + (16 * m) * 68 + 16 * j + c;
+  if (w == 0) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) acc += Ar[q] * Tc[q * 68];
+    for (int i = 1; i < 4; ++i) {
+      const int R = 16 * i;
+      // S (16 x 16i) = A[R:R+16, 0:16i] * Tf[0:16i, 0:16i]; S stored fp32, ld 52
+      for (int nt = 0; nt < 2 * i; ++nt) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kt = 0; kt < 2 * i; ++kt) {
+          uint32_t a[4];
+          a[0] = to_tf32(A[(R + g) * 68 + 8 * kt + t]);
+          a[1] = to_tf32(A[(R + g + 8) * 68 + 8 * kt + t]);
+          a[2] = to_tf32(A[(R + g) * 68 + 8 * kt + t + 4]);
+          a[3] = to_tf32(A[(R + g + 8) * 68 + 8 * kt + t + 4]);
+          const uint32_t b0 = to_tf32(Tf[(8 * kt + t) * 68 + 8 * nt + g]);
+          const uint32_t b1 = to_tf32(Tf[(8 * kt + t + 4) * 68 + 8 * nt + g]);
+          mma_tf32(acc, a, b0, b1);
+        }
+        S[g * 52 + 8 * nt + 2 * t] = acc[0];
+        S[g * 52 + 8 * nt + 2 * t + 1] = acc[1];
+        S[(g + 8) * 52 + 8 * nt + 2 * t] = acc[2];
+        S[(g + 8) * 52 + 8 * nt + 2 * t + 1] = acc[3];
       }
-      S[j * 272 + r * 17 + c] = acc;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < i * 256; idx += NT) {
-      const int j = idx >> 8, e = idx & 255, r = e >> 4, c = e & 15;
-      const float* Tr = Tf + (16 * i + r) * 68 + 16 * i;
-      float acc = 0.f;
+      __syncwarp();
+      // T[R:R+16, 0:16i] = -T_ii S
+      for (int nt = 0; nt < 2 * i; ++nt) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q = 0; q < 16; ++q) acc += (q <= r) ? Tr[q] * S[j * 272 + q * 17 + c] : 0.f;
-      Tf[(16 * i + r) * 68 + 16 * j + c] = -acc;
+        for (int kt = 0; kt < 2; ++kt) {
+          uint32_t a[4];
+          a[0] = to_tf32(Tf[(R + g) * 68 + R + 8 * kt + t]);
+          a[1] = to_tf32(Tf[(R + g + 8) * 68 + R + 8 * kt + t]);
+          a[2] = to_tf32(Tf[(R + g) * 68 + R + 8 * kt + t + 4]);
+          a[3] = to_tf32(Tf[(R + g + 8) * 68 + R + 8 * kt + t + 4]);
+          const uint32_t b0 = to_tf32(S[(8 * kt + t) * 52 + 8 * nt + g]);
+          const uint32_t b1 = to_tf32(S[(8 * kt + t + 4) * 52 + 8 * nt + g]);
+          mma_tf32(acc, a, b0, b1);
+        }
+        Tf[(R + g) * 68 + 8 * nt + 2 * t] = -acc[0];
+        Tf[(R + g) * 68 + 8 * nt + 2 * t + 1] = -acc[1];
+        Tf[(R + g + 8) * 68 + 8 * nt + 2 * t] = -acc[2];
+        Tf[(R + g + 8) * 68 + 8 * nt + 2 * t + 1] = -acc[3];
+      }
+      __syncwarp();
     }
-    __syncthreads();
   }
+  __syncthreads();
 }
 
 // 8 warps; warp (rw = w & 3, cw = w >> 2) owns rows [16 rw, 16 rw + 16) and
@@ -205,8 +231,12 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
         const float d0 = (c <= r) ? __expf(gr - sm.g[c]) : 0.f;
         const float d1 = (c + 1 <= r) ? __expf(gr - sm.g[c + 1]) : 0.f;
         const float br = sm.b[r];
-        sA[r * 68 + c] = (c < r) ? br * kk[j][2 * hf] * d0 : 0.f;
-        sA[r * 68 + c + 1] = (c + 1 < r) ? br * kk[j][2 * hf + 1] * d1 : 0.f;
+        const float km0 = (c < r) ? kk[j][2 * hf] * d0 : 0.f;
+        const float km1 = (c + 1 < r) ? kk[j][2 * hf + 1] * d1 : 0.f;
+        sA[r * 68 + c] = br * km0;
+        sA[r * 68 + c + 1] = br * km1;
+        if (ws.KKM)
+          *reinterpret_cast<uint32_t*>(ws.KKM + bh * BT * LD64 + r * LD64 + c) = pack_bf16(km0, km1);
         *reinterpret_cast<uint32_t*>(qkm + r * LD64 + c) =
             pack_bf16(qk[j][2 * hf] * d0, qk[j][2 * hf + 1] * d1);
       }
