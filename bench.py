@@ -33,6 +33,27 @@ UNIT = "tokens/s"
 WORKLOAD_INDEX = 2
 
 
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture
+    (profiles/kernel_dram_traffic.json), or None if the kernel's source has
+    changed since the counters were taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "kernel_dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+        def sha(rel):
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                return hashlib.sha256(f.read()).hexdigest()
+        common = "chunked_linear_recurrence_gated_gb300/csrc/gdn_common.cuh"
+        if sha(rec["source"]) != rec["source_sha256"] or sha(common) != rec["common_sha256"]:
+            return None
+        return rec["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -313,7 +334,7 @@ def reference_arm(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -363,6 +384,11 @@ def main():
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        t_start = time.perf_counter()
+        while time.perf_counter() - t_start < 0.6:  # let the clock sampler start under load
+            runner.step()
+            torch.cuda.synchronize(dev)
+        barrier(world)
         ms = time_steps(runner.step, args.steps, dev)
     barrier(world)
     ms_step, value = aggregate(ms / args.steps, w.B * w.T, world, device=dev)
@@ -394,8 +420,10 @@ def main():
                     "peak_source": "derived: fp32 FFMA lanes x max clock"}
         else:
             achieved = by * nblk_heads / (avg_ms / 1e3) / 1e9
+            traffic = measured_traffic(dom) if nblk_heads == 512 * 16 else None
             roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "traffic": None, "kernel": dom,
+                    "frac": achieved / hbm, "traffic": traffic, "kernel": dom,
+                    "alg_bytes_per_launch": by * nblk_heads, "launch_ms": avg_ms,
                     "peak_source": peak_kind}
     else:
         roof = {"bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
