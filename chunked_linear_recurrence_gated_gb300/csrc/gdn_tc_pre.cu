@@ -59,7 +59,8 @@ __device__ __forceinline__ void block_cumsum64(float* sg) {
 
 // T = (I + A)^-1 for strictly-lower 64 x 64 A (fp32, ld 68), NT threads.
 // The four diagonal 16 x 16 blocks by fp32 forward substitution (one warp
-// each); then, block row by block row (i = 1..3), warp 0 forms
+// each); then, block row by block row (i = 1..3), warps 0..2i-1 (one n8
+// column tile each) form
 //   S = A[i, 0:i] T[0:i, 0:i]   and   T[i, 0:i] = -T_ii S
 // with TF32 tensor-core MMAs (fp32 accumulation): the block products of
 // T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj for all j < i at once.
@@ -82,52 +83,51 @@ __device__ void invert_unit_lower64(const float* A, float* Tf, float* S) {
     }
   }
   __syncthreads();
-  if (w == 0) {
+  // block row i: warp w < 2i owns the n8 column tile w of both products, so the
+  // two products of a level need no barrier between them (each warp reads back
+  // only its own S columns); one barrier per level publishes the new rows.
 #pragma unroll
-    for (int i = 1; i < 4; ++i) {
-      const int R = 16 * i;
-      // S (16 x 16i) = A[R:R+16, 0:16i] * Tf[0:16i, 0:16i]; S stored fp32, ld 52
-      for (int nt = 0; nt < 2 * i; ++nt) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int kt = 0; kt < 2 * i; ++kt) {
-          uint32_t a[4];
-          a[0] = to_tf32(A[(R + g) * 68 + 8 * kt + t]);
-          a[1] = to_tf32(A[(R + g + 8) * 68 + 8 * kt + t]);
-          a[2] = to_tf32(A[(R + g) * 68 + 8 * kt + t + 4]);
-          a[3] = to_tf32(A[(R + g + 8) * 68 + 8 * kt + t + 4]);
-          const uint32_t b0 = to_tf32(Tf[(8 * kt + t) * 68 + 8 * nt + g]);
-          const uint32_t b1 = to_tf32(Tf[(8 * kt + t + 4) * 68 + 8 * nt + g]);
-          mma_tf32(acc, a, b0, b1);
-        }
-        S[g * 52 + 8 * nt + 2 * t] = acc[0];
-        S[g * 52 + 8 * nt + 2 * t + 1] = acc[1];
-        S[(g + 8) * 52 + 8 * nt + 2 * t] = acc[2];
-        S[(g + 8) * 52 + 8 * nt + 2 * t + 1] = acc[3];
+  for (int i = 1; i < 4; ++i) {
+    const int R = 16 * i;
+    if (w < 2 * i) {
+      const int nt = w;
+      // S (16 x 8, column tile nt) = A[R:R+16, 0:16i] * Tf[0:16i, 8nt:8nt+8]; fp32, ld 52
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kt = 0; kt < 2 * i; ++kt) {
+        uint32_t a[4];
+        a[0] = to_tf32(A[(R + g) * 68 + 8 * kt + t]);
+        a[1] = to_tf32(A[(R + g + 8) * 68 + 8 * kt + t]);
+        a[2] = to_tf32(A[(R + g) * 68 + 8 * kt + t + 4]);
+        a[3] = to_tf32(A[(R + g + 8) * 68 + 8 * kt + t + 4]);
+        const uint32_t b0 = to_tf32(Tf[(8 * kt + t) * 68 + 8 * nt + g]);
+        const uint32_t b1 = to_tf32(Tf[(8 * kt + t + 4) * 68 + 8 * nt + g]);
+        mma_tf32(acc, a, b0, b1);
       }
+      S[g * 52 + 8 * nt + 2 * t] = acc[0];
+      S[g * 52 + 8 * nt + 2 * t + 1] = acc[1];
+      S[(g + 8) * 52 + 8 * nt + 2 * t] = acc[2];
+      S[(g + 8) * 52 + 8 * nt + 2 * t + 1] = acc[3];
       __syncwarp();
-      // T[R:R+16, 0:16i] = -T_ii S
-      for (int nt = 0; nt < 2 * i; ++nt) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // T[R:R+16, 8nt:8nt+8] = -T_ii S
+      float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kt = 0; kt < 2; ++kt) {
-          uint32_t a[4];
-          a[0] = to_tf32(Tf[(R + g) * 68 + R + 8 * kt + t]);
-          a[1] = to_tf32(Tf[(R + g + 8) * 68 + R + 8 * kt + t]);
-          a[2] = to_tf32(Tf[(R + g) * 68 + R + 8 * kt + t + 4]);
-          a[3] = to_tf32(Tf[(R + g + 8) * 68 + R + 8 * kt + t + 4]);
-          const uint32_t b0 = to_tf32(S[(8 * kt + t) * 52 + 8 * nt + g]);
-          const uint32_t b1 = to_tf32(S[(8 * kt + t + 4) * 52 + 8 * nt + g]);
-          mma_tf32(acc, a, b0, b1);
-        }
-        Tf[(R + g) * 68 + 8 * nt + 2 * t] = -acc[0];
-        Tf[(R + g) * 68 + 8 * nt + 2 * t + 1] = -acc[1];
-        Tf[(R + g + 8) * 68 + 8 * nt + 2 * t] = -acc[2];
-        Tf[(R + g + 8) * 68 + 8 * nt + 2 * t + 1] = -acc[3];
+      for (int kt = 0; kt < 2; ++kt) {
+        uint32_t a[4];
+        a[0] = to_tf32(Tf[(R + g) * 68 + R + 8 * kt + t]);
+        a[1] = to_tf32(Tf[(R + g + 8) * 68 + R + 8 * kt + t]);
+        a[2] = to_tf32(Tf[(R + g) * 68 + R + 8 * kt + t + 4]);
+        a[3] = to_tf32(Tf[(R + g + 8) * 68 + R + 8 * kt + t + 4]);
+        const uint32_t b0 = to_tf32(S[(8 * kt + t) * 52 + 8 * nt + g]);
+        const uint32_t b1 = to_tf32(S[(8 * kt + t + 4) * 52 + 8 * nt + g]);
+        mma_tf32(acc2, a, b0, b1);
       }
-      __syncwarp();
+      Tf[(R + g) * 68 + 8 * nt + 2 * t] = -acc2[0];
+      Tf[(R + g) * 68 + 8 * nt + 2 * t + 1] = -acc2[1];
+      Tf[(R + g + 8) * 68 + 8 * nt + 2 * t] = -acc2[2];
+      Tf[(R + g + 8) * 68 + 8 * nt + 2 * t + 1] = -acc2[3];
     }
+    __syncthreads();
   }
-  __syncthreads();
 }
 
 // 8 warps; warp (rw = w & 3, cw = w >> 2) owns rows [16 rw, 16 rw + 16) and
