@@ -180,7 +180,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- the step
 class Runner:
-    def __init__(self, w, dev, seed_offset=0):
+    def __init__(self, w, dev, seed_offset=0, reuse=True):
         from chunked_linear_recurrence_gated_gb300 import gdn
         from chunked_linear_recurrence_gated_gb300.inputs import make_workload_inputs
 
@@ -203,8 +203,17 @@ class Runner:
         self.bounds = np.concatenate([[0], np.cumsum(w.chunks)]).astype(int)
         Lmax = max(w.chunks)
         shp = gdn.gdn_shape(B, Lmax, H, dk, dv, 1 if w.dtype == "bf16" else 0)
-        self.ws_f = gdn.alloc_workspace(gdn.chunk_workspace_bytes(shp, False), dev)
-        self.ws_b = gdn.alloc_workspace(gdn.chunk_workspace_bytes(shp, True), dev)
+        self.reuse = reuse
+        if reuse:
+            # the backward reads the per-block products its chunk's forward kept
+            self.ws_s = gdn.alloc_workspace(gdn.chunk_workspace_bytes(shp, gdn.GDN_WS_SAVED), dev)
+            self.saved = []
+            for L in w.chunks:
+                s_i = gdn.gdn_shape(B, int(L), H, dk, dv, shp.dtype)
+                self.saved.append(gdn.alloc_workspace(gdn.chunk_saved_bytes(s_i), dev))
+        else:
+            self.ws_f = gdn.alloc_workspace(gdn.chunk_workspace_bytes(shp, False), dev)
+            self.ws_b = gdn.alloc_workspace(gdn.chunk_workspace_bytes(shp, True), dev)
         self.launches_per_step = None
 
     def sl(self, t, i):
@@ -214,16 +223,27 @@ class Runner:
         g, x = self.gdn, self.x
         n = len(self.w.chunks)
         for i in range(n):
-            g.gdn_chunk_fwd(self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
-                            self.sl(x["g"], i), self.sl(x["beta"], i), S_in=self.S[i],
-                            o=self.sl(self.o, i), S_out=self.S[i + 1], workspace=self.ws_f)
+            args = (self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
+                    self.sl(x["g"], i), self.sl(x["beta"], i))
+            if self.reuse:
+                g.gdn_chunk_fwd_save(*args, S_in=self.S[i], saved=self.saved[i],
+                                     o=self.sl(self.o, i), S_out=self.S[i + 1],
+                                     workspace=self.ws_s)
+            else:
+                g.gdn_chunk_fwd(*args, S_in=self.S[i], o=self.sl(self.o, i),
+                                S_out=self.S[i + 1], workspace=self.ws_f)
         for i in reversed(range(n)):
-            g.gdn_chunk_bwd(self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
-                            self.sl(x["g"], i), self.sl(x["beta"], i), self.S[i],
-                            self.sl(x["do"], i), dS_out=self.dS[i + 1] if i + 1 < n else None,
-                            grads=(self.sl(self.dq, i), self.sl(self.dk, i), self.sl(self.dv, i),
-                                   self.sl(self.dg, i), self.sl(self.db, i)),
-                            dS_in=self.dS[i], workspace=self.ws_b)
+            args = (self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
+                    self.sl(x["g"], i), self.sl(x["beta"], i), self.S[i], self.sl(x["do"], i))
+            grads = (self.sl(self.dq, i), self.sl(self.dk, i), self.sl(self.dv, i),
+                     self.sl(self.dg, i), self.sl(self.db, i))
+            dS_out = self.dS[i + 1] if i + 1 < n else None
+            if self.reuse:
+                g.gdn_chunk_bwd_saved(*args, self.saved[i], dS_out=dS_out, grads=grads,
+                                      dS_in=self.dS[i], workspace=self.ws_s)
+            else:
+                g.gdn_chunk_bwd(*args, dS_out=dS_out, grads=grads, dS_in=self.dS[i],
+                                workspace=self.ws_b)
 
 
 def barrier(world):
@@ -341,6 +361,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
                     help="workload index (1-3: fixed-length chunked bf16 workloads)")
+    ap.add_argument("--recompute", action="store_true",
+                    help="backward recomputes the per-block Pre products instead of reading "
+                         "the ones its chunk's forward kept")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run only the first N tokens (a whole number of chunks); "
                          "for small profiling cases")
@@ -378,7 +401,7 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
 
-    runner = Runner(w, dev)
+    runner = Runner(w, dev, reuse=not args.recompute)
     for _ in range(max(args.warmup, 3)):
         runner.step()
     barrier(world)
@@ -455,6 +478,8 @@ def main():
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk,
                        "dv": w.dv, "chunks": w.chunks, "state": "fp32",
+                       "backward": ("recomputes the Pre products" if args.recompute else
+                                    "reads the Pre products its chunk's forward kept"),
                        "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"dp{world} (independent sequence per GPU)"},
             "clocks": clk.summary(),

@@ -164,31 +164,20 @@ size_t simt_layout(const Plan& p, bool bwd, SimtWs* ws, int** blk0, int** blk_se
 }
 
 // Workspace layout of the tensor-core kernels (bf16 intermediates).
-size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, char* base) {
-  Carve c;
+// Per-block products of the Pre kernel (dec, W, U, QKM, Kp, Qp; the backward
+// also T and KKM), carved from `base` (nullptr: sizes only) starting at offset 0.
+void carve_pre(const Plan& p, bool bwd, Carve& c, TcWs* ws, char* base) {
+  using bf = __nv_bfloat16;
   const size_t nbh = (size_t)p.nblk_cap * p.H;
-  const size_t o_status = c.take(kAlign);
-  const size_t o_blk0 = p.varlen ? c.take(sizeof(int) * (p.nseq + 1)) : 0;
-  const size_t o_blks = p.varlen ? c.take(sizeof(int) * (size_t)p.nblk_cap) : 0;
   const size_t o_dec = c.take(4 * nbh * 3 * BT);
   const size_t o_W = c.take(2 * nbh * BT * TC_LDK);
   const size_t o_U = c.take(2 * nbh * (p.dv / 16) * BT * TC_LDU);
   const size_t o_QKM = c.take(2 * nbh * BT * TC_LD64);
   const size_t o_Kp = c.take(2 * nbh * BT * TC_LDK);
   const size_t o_Qp = c.take(2 * nbh * BT * TC_LDK);
-  size_t o_T = 0, o_Hb = 0, o_Vn = 0, o_dH = 0, o_dVn = 0;
-  size_t o_KKM = 0;
-  if (bwd) {
-    o_T = c.take(2 * nbh * BT * BT);
-    o_KKM = c.take(2 * nbh * BT * TC_LD64);
-    o_Hb = c.take(2 * nbh * p.dv * p.dk);
-    o_Vn = c.take(2 * nbh * p.dv * BT);
-    o_dH = c.take(2 * nbh * p.dv * p.dk);
-    o_dVn = c.take(2 * nbh * p.dv * BT);
-  }
+  const size_t o_T = bwd ? c.take(2 * nbh * BT * BT) : 0;
+  const size_t o_KKM = bwd ? c.take(2 * nbh * BT * TC_LD64) : 0;
   if (base) {
-    using bf = __nv_bfloat16;
-    ws->status = (int*)(base + o_status);
     ws->dec = (float*)(base + o_dec);
     ws->W = (bf*)(base + o_W);
     ws->U = (bf*)(base + o_U);
@@ -197,6 +186,46 @@ size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, c
     ws->Qp = (bf*)(base + o_Qp);
     ws->T = bwd ? (bf*)(base + o_T) : nullptr;
     ws->KKM = bwd ? (bf*)(base + o_KKM) : nullptr;
+  }
+}
+
+// Bytes of the saved forward products (gdn_chunk_fwd_save / gdn_chunk_bwd_saved).
+size_t saved_layout(const Plan& p, TcWs* ws, char* base) {
+  Carve c;
+  carve_pre(p, true, c, ws, base);
+  return c.off;
+}
+
+// Workspace layout of the tensor-core kernels. The first 256 bytes hold the
+// status word. WS_FWD / WS_BWD hold the Pre products themselves; WS_SAVED
+// leaves them to a separate saved-products buffer.
+enum WsKind { WS_FWD = 0, WS_BWD = 1, WS_SAVED = 2 };
+size_t tc_layout(const Plan& p, int kind, TcWs* ws, int** blk0, int** blk_seq, char* base) {
+  Carve c;
+  const bool bwd = kind != WS_FWD;
+  const size_t nbh = (size_t)p.nblk_cap * p.H;
+  const size_t o_status = c.take(kAlign);
+  const size_t o_blk0 = p.varlen ? c.take(sizeof(int) * (p.nseq + 1)) : 0;
+  const size_t o_blks = p.varlen ? c.take(sizeof(int) * (size_t)p.nblk_cap) : 0;
+  if (kind != WS_SAVED) {
+    Carve pc;
+    carve_pre(p, bwd, pc, ws, nullptr);
+    const size_t o_pre = c.take(pc.off);
+    if (base) {
+      Carve pb;
+      carve_pre(p, bwd, pb, ws, base + o_pre);
+    }
+  }
+  size_t o_Hb = 0, o_Vn = 0, o_dH = 0, o_dVn = 0;
+  if (bwd) {
+    o_Hb = c.take(2 * nbh * p.dv * p.dk);
+    o_Vn = c.take(2 * nbh * p.dv * BT);
+    o_dH = c.take(2 * nbh * p.dv * p.dk);
+    o_dVn = c.take(2 * nbh * p.dv * BT);
+  }
+  if (base) {
+    using bf = __nv_bfloat16;
+    ws->status = (int*)(base + o_status);
     ws->HbT = bwd ? (bf*)(base + o_Hb) : nullptr;
     ws->VnT = bwd ? (bf*)(base + o_Vn) : nullptr;
     ws->dHT = bwd ? (bf*)(base + o_dH) : nullptr;
@@ -207,14 +236,22 @@ size_t tc_layout(const Plan& p, bool bwd, TcWs* ws, int** blk0, int** blk_seq, c
   return c.off;
 }
 
-size_t ws_bytes(const Plan& p, bool bwd) {
+size_t ws_bytes(const Plan& p, int kind) {
   int *a, *b;
   if (path_of(p) == 2) {
     TcWs w;
-    return tc_layout(p, bwd, &w, &a, &b, nullptr);
+    return tc_layout(p, kind, &w, &a, &b, nullptr);
   }
   SimtWs w;
-  return simt_layout(p, bwd, &w, &a, &b, nullptr);
+  return simt_layout(p, kind != WS_FWD, &w, &a, &b, nullptr);
+}
+
+size_t saved_bytes(const Plan& p) {
+  if (path_of(p) == 2) {
+    TcWs w;
+    return saved_layout(p, &w, nullptr);
+  }
+  return kAlign;  // the fp32 SIMT kernels keep nothing between the two calls
 }
 
 bool al(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
@@ -239,9 +276,11 @@ SeqMap make_map(const Plan& p, const int* cu, const int* blk0, const int* blk_se
   return m;
 }
 
+// `saved` (nullable): the forward also keeps its Pre products there, with the
+// backward's T and K K^T tiles, for run_bwd to read instead of recomputing.
 gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, void* o, float* S_out,
-                   void* ws, size_t wsb, void* stream) {
+                   void* saved, size_t savedb, void* ws, size_t wsb, void* stream) {
   const size_t esz = p.dtype == GDN_DTYPE_F32 ? 4 : 2;
   const bool any = p.T > 0;
   if (!check_tensor(q, any, 16) || !check_tensor(k, any, 16) || !check_tensor(v, any, 16) ||
@@ -249,13 +288,19 @@ gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, c
       !check_tensor(S_in, false, 16) || !check_tensor(S_out, false, 16))
     return GDN_ERR_INVALID_ARG;
   if (p.varlen && (!cu || !al(cu, 4))) return GDN_ERR_INVALID_ARG;
-  if (!ws || !al(ws, kAlign) || wsb < ws_bytes(p, false)) return GDN_ERR_WORKSPACE;
+  const int kind = saved ? WS_SAVED : WS_FWD;
+  if (!ws || !al(ws, kAlign) || wsb < ws_bytes(p, kind)) return GDN_ERR_WORKSPACE;
+  if (saved && (!al(saved, kAlign) || savedb < saved_bytes(p))) return GDN_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
   int *blk0, *blk_seq;
   cudaError_t e;
   if (path_of(p) == 2) {
     TcWs w;
-    tc_layout(p, false, &w, &blk0, &blk_seq, (char*)ws);
+    tc_layout(p, kind, &w, &blk0, &blk_seq, (char*)ws);
+    if (saved) {
+      saved_layout(p, &w, (char*)saved);
+      w.HbT = w.VnT = w.dHT = w.dVnT = nullptr;
+    }
     if (p.varlen && (e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st)))
       return GDN_ERR_CUDA;
     const SeqMap m = make_map(p, cu, blk0, blk_seq);
@@ -264,6 +309,7 @@ gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, c
   }
   SimtWs w;
   simt_layout(p, false, &w, &blk0, &blk_seq, (char*)ws);
+  (void)savedb;
   if (p.varlen)
     e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st);
   else {
@@ -277,10 +323,13 @@ gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, c
   return e ? GDN_ERR_CUDA : GDN_OK;
 }
 
+// `saved` (nullable): Pre products written by run_fwd on the same inputs; the
+// Pre kernel is then not launched again.
 gdn_status run_bwd(const Plan& p, const int* cu, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, const void* dout,
                    const float* dS_out, void* dq, void* dk, void* dv, void* dg, void* dbeta,
-                   float* dS_in, void* ws, size_t wsb, void* stream) {
+                   float* dS_in, const void* saved, size_t savedb, void* ws, size_t wsb,
+                   void* stream) {
   const size_t esz = p.dtype == GDN_DTYPE_F32 ? 4 : 2;
   const bool any = p.T > 0;
   if (!check_tensor(q, any, 16) || !check_tensor(k, any, 16) || !check_tensor(v, any, 16) ||
@@ -291,17 +340,21 @@ gdn_status run_bwd(const Plan& p, const int* cu, const void* q, const void* k, c
       !check_tensor(dS_out, false, 16) || !check_tensor(dS_in, false, 16))
     return GDN_ERR_INVALID_ARG;
   if (p.varlen && (!cu || !al(cu, 4))) return GDN_ERR_INVALID_ARG;
-  if (!ws || !al(ws, kAlign) || wsb < ws_bytes(p, true)) return GDN_ERR_WORKSPACE;
+  const int kind = saved ? WS_SAVED : WS_BWD;
+  if (!ws || !al(ws, kAlign) || wsb < ws_bytes(p, kind)) return GDN_ERR_WORKSPACE;
+  if (saved && (!al(saved, kAlign) || savedb < saved_bytes(p))) return GDN_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
   int *blk0, *blk_seq;
   cudaError_t e;
   if (path_of(p) == 2) {
     TcWs w;
-    tc_layout(p, true, &w, &blk0, &blk_seq, (char*)ws);
+    tc_layout(p, kind, &w, &blk0, &blk_seq, (char*)ws);
+    if (saved) saved_layout(p, &w, (char*)saved);
     if (p.varlen && (e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st)))
       return GDN_ERR_CUDA;
     const SeqMap m = make_map(p, cu, blk0, blk_seq);
-    e = tc_bwd(m, p.dv, q, k, v, g, beta, S_in, dout, dS_out, dq, dk, dv, dg, dbeta, dS_in, w, st);
+    e = tc_bwd(m, p.dv, q, k, v, g, beta, S_in, dout, dS_out, dq, dk, dv, dg, dbeta, dS_in, w,
+               saved == nullptr, st);
     return e ? GDN_ERR_CUDA : GDN_OK;
   }
   SimtWs w;
@@ -327,13 +380,14 @@ extern "C" {
 size_t gdn_chunk_workspace_bytes(const gdn_shape* shape, int is_bwd) {
   Plan p;
   if (plan_shape(shape, false, 0, &p) != GDN_OK) return 0;
-  return ws_bytes(p, is_bwd != 0);
+  if (is_bwd != GDN_WS_SAVED) is_bwd = is_bwd != 0 ? WS_BWD : WS_FWD;
+  return ws_bytes(p, is_bwd);
 }
 
 size_t gdn_varlen_workspace_bytes(const gdn_shape* shape, int nseq, int is_bwd) {
   Plan p;
   if (plan_shape(shape, true, nseq, &p) != GDN_OK) return 0;
-  return ws_bytes(p, is_bwd != 0);
+  return ws_bytes(p, is_bwd != 0 ? WS_BWD : WS_FWD);
 }
 
 gdn_status gdn_chunk_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
@@ -342,8 +396,40 @@ gdn_status gdn_chunk_fwd(const gdn_shape* shape, const void* q, const void* k, c
   Plan p;
   gdn_status s = plan_shape(shape, false, 0, &p);
   if (s != GDN_OK) return s;
-  return run_fwd(p, nullptr, q, k, v, g, beta, S_in, o, S_out, workspace, workspace_bytes,
-                 stream);
+  return run_fwd(p, nullptr, q, k, v, g, beta, S_in, o, S_out, nullptr, 0, workspace,
+                 workspace_bytes, stream);
+}
+
+size_t gdn_chunk_saved_bytes(const gdn_shape* shape) {
+  Plan p;
+  if (plan_shape(shape, false, 0, &p) != GDN_OK) return 0;
+  return saved_bytes(p);
+}
+
+gdn_status gdn_chunk_fwd_save(const gdn_shape* shape, const void* q, const void* k,
+                              const void* v, const void* g, const void* beta, const float* S_in,
+                              void* o, float* S_out, void* saved, size_t saved_bytes_,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  Plan p;
+  gdn_status s = plan_shape(shape, false, 0, &p);
+  if (s != GDN_OK) return s;
+  if (!saved) return GDN_ERR_WORKSPACE;
+  return run_fwd(p, nullptr, q, k, v, g, beta, S_in, o, S_out, saved, saved_bytes_, workspace,
+                 workspace_bytes, stream);
+}
+
+gdn_status gdn_chunk_bwd_saved(const gdn_shape* shape, const void* q, const void* k,
+                               const void* v, const void* g, const void* beta,
+                               const float* S_in, const void* dout, const float* dS_out,
+                               void* dq, void* dk, void* dv, void* dg, void* dbeta, float* dS_in,
+                               const void* saved, size_t saved_bytes_, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  Plan p;
+  gdn_status s = plan_shape(shape, false, 0, &p);
+  if (s != GDN_OK) return s;
+  if (!saved) return GDN_ERR_WORKSPACE;
+  return run_bwd(p, nullptr, q, k, v, g, beta, S_in, dout, dS_out, dq, dk, dv, dg, dbeta, dS_in,
+                 saved, saved_bytes_, workspace, workspace_bytes, stream);
 }
 
 gdn_status gdn_chunk_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
@@ -355,7 +441,7 @@ gdn_status gdn_chunk_bwd(const gdn_shape* shape, const void* q, const void* k, c
   gdn_status s = plan_shape(shape, false, 0, &p);
   if (s != GDN_OK) return s;
   return run_bwd(p, nullptr, q, k, v, g, beta, S_in, dout, dS_out, dq, dk, dv, dg, dbeta, dS_in,
-                 workspace, workspace_bytes, stream);
+                 nullptr, 0, workspace, workspace_bytes, stream);
 }
 
 gdn_status gdn_varlen_fwd(const gdn_shape* shape, const int* cu_seqlens, int nseq,
@@ -365,8 +451,8 @@ gdn_status gdn_varlen_fwd(const gdn_shape* shape, const int* cu_seqlens, int nse
   Plan p;
   gdn_status s = plan_shape(shape, true, nseq, &p);
   if (s != GDN_OK) return s;
-  return run_fwd(p, cu_seqlens, q, k, v, g, beta, S0, o, S_final, workspace, workspace_bytes,
-                 stream);
+  return run_fwd(p, cu_seqlens, q, k, v, g, beta, S0, o, S_final, nullptr, 0, workspace,
+                 workspace_bytes, stream);
 }
 
 gdn_status gdn_varlen_bwd(const gdn_shape* shape, const int* cu_seqlens, int nseq,
@@ -379,7 +465,7 @@ gdn_status gdn_varlen_bwd(const gdn_shape* shape, const int* cu_seqlens, int nse
   gdn_status s = plan_shape(shape, true, nseq, &p);
   if (s != GDN_OK) return s;
   return run_bwd(p, cu_seqlens, q, k, v, g, beta, S0, dout, dS_final, dq, dk, dv, dg, dbeta,
-                 dS0, workspace, workspace_bytes, stream);
+                 dS0, nullptr, 0, workspace, workspace_bytes, stream);
 }
 
 const char* gdn_status_str(gdn_status status) {

@@ -23,14 +23,16 @@ cudaError_t tc_pre(const SeqMap& m, int dv, const void* q, const void* k, const 
 cudaError_t tc_grad(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
                     const void* beta, const void* dout, void* dq, void* dk_out, void* dv_out,
                     void* dg, void* dbeta, const TcWs& ws, cudaStream_t st);
-// Whole forward / backward calls (gdn_tc_chain.cu).
+// Whole forward / backward calls (gdn_tc_chain.cu). The backward skips the Pre
+// kernel when run_pre is false: ws then points at Pre products (with T and
+// K K^T) that a forward call wrote for the same inputs.
 cudaError_t tc_fwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, void* o, float* S_out,
                    const TcWs& ws, cudaStream_t st);
 cudaError_t tc_bwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, const void* dout,
                    const float* dS_out, void* dq, void* dk_out, void* dv_out, void* dg,
-                   void* dbeta, float* dS_in, const TcWs& ws, cudaStream_t st);
+                   void* dbeta, float* dS_in, const TcWs& ws, bool run_pre, cudaStream_t st);
 
 // Diagnostic timing hook (include/gdn_profile.h): records an event before the
 // kernel named `next` (nullptr after the last kernel of a call) when armed.

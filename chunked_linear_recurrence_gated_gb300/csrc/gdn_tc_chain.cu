@@ -647,10 +647,10 @@ template <int DV>
 cudaError_t bwd_t(const SeqMap& m, const void* q, const void* k, const void* v, const void* g,
                   const void* beta, const float* S_in, const void* dout, const float* dS_out,
                   void* dq, void* dkk, void* dvv, void* dg, void* dbeta, float* dS_in,
-                  const TcWs& ws, cudaStream_t st) {
+                  const TcWs& ws, bool run_pre, cudaStream_t st) {
   using bf = __nv_bfloat16;
   cudaError_t e;
-  if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, st))) return e;
+  if (run_pre && (e = tc_pre(m, DV, q, k, v, g, beta, ws, st))) return e;
   constexpr size_t s1 = sizeof(FwdSmem<CHAIN_RECOMPUTE, BWD_RG>);
   constexpr size_t s2 = sizeof(RevSmem<BWD_RG>);
   constexpr size_t smem = s1 > s2 ? s1 : s2;
@@ -677,12 +677,12 @@ cudaError_t tc_fwd(const SeqMap& m, int dv, const void* q, const void* k, const 
 cudaError_t tc_bwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, const void* dout,
                    const float* dS_out, void* dq, void* dkk, void* dvv, void* dg, void* dbeta,
-                   float* dS_in, const TcWs& ws, cudaStream_t st) {
+                   float* dS_in, const TcWs& ws, bool run_pre, cudaStream_t st) {
   if (dv == 128)
     return bwd_t<128>(m, q, k, v, g, beta, S_in, dout, dS_out, dq, dkk, dvv, dg, dbeta, dS_in, ws,
-                      st);
+                      run_pre, st);
   return bwd_t<256>(m, q, k, v, g, beta, S_in, dout, dS_out, dq, dkk, dvv, dg, dbeta, dS_in, ws,
-                    st);
+                    run_pre, st);
 }
 
 }  // namespace gdn

@@ -192,9 +192,17 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       }
     }
     // <dH, H_b> partial
-    for (int idx = tid; idx < VC * DK; idx += 256) {
-      const int r = idx >> 7, cc = idx & 127;
-      hd += __bfloat162float(C.dHT[r * LDK + cc]) * __bfloat162float(C.HbT[r * LDK + cc]);
+    for (int idx = tid; idx < VC * DK / 8; idx += 256) {
+      const int r = idx >> 4, cc = (idx & 15) * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(&C.dHT[r * LDK + cc]);
+      const uint4 b = *reinterpret_cast<const uint4*>(&C.HbT[r * LDK + cc]);
+      const uint32_t* ap = &a.x;
+      const uint32_t* bp = &b.x;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = unpack_bf16(ap[e]), y = unpack_bf16(bp[e]);
+        hd += x.x * y.x + x.y * y.y;
+      }
     }
     // Y = T^T dV^new on this chunk (warp: rows R0.., value columns 16 cw..): dv = beta Y, dbeta += Y . V
     {

@@ -26,7 +26,9 @@ _STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
 EXPORTS = ["gdn_chunk_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "gdn_varlen_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd",
            "gdn_status_str", "gdn_workspace_status", "gdn_path", "gdn_version",
-           "gdn_chunk_fwd_noalloc"]
+           "gdn_chunk_fwd_noalloc", "gdn_chunk_saved_bytes", "gdn_chunk_fwd_save",
+           "gdn_chunk_bwd_saved"]
+GDN_WS_SAVED = 2
 
 
 class GdnError(RuntimeError):
@@ -81,6 +83,12 @@ def load(build_if_missing: bool = False):
     lib.gdn_version.restype = I
     lib.gdn_chunk_fwd_noalloc.argtypes = [SP] + [P] * 8 + [P]
     lib.gdn_chunk_fwd_noalloc.restype = I
+    lib.gdn_chunk_saved_bytes.argtypes = [SP]
+    lib.gdn_chunk_saved_bytes.restype = Z
+    lib.gdn_chunk_fwd_save.argtypes = [SP] + [P] * 8 + [P, Z, P, Z, P]
+    lib.gdn_chunk_fwd_save.restype = I
+    lib.gdn_chunk_bwd_saved.argtypes = [SP] + [P] * 14 + [P, Z, P, Z, P]
+    lib.gdn_chunk_bwd_saved.restype = I
     lib.gdn_profile_arm.argtypes = [P, I]
     lib.gdn_profile_arm.restype = None
     lib.gdn_profile_count.argtypes = []
@@ -179,6 +187,58 @@ def gdn_chunk_bwd(q, k, v, g, beta, S_in, dout, dS_out=None, grads=None, dS_in=N
                            _p(dout), _p(dS_out), *[_p(t) for t in grads], _p(dS_in),
                            _p(workspace), workspace.numel(), _stream(stream))
     _check(rc, "gdn_chunk_bwd")
+    return (*grads, dS_in)
+
+
+def chunk_saved_bytes(shape: gdn_shape) -> int:
+    return load().gdn_chunk_saved_bytes(ctypes.byref(shape))
+
+
+def gdn_chunk_fwd_save(q, k, v, g, beta, S_in=None, saved=None, o=None, S_out=None,
+                       workspace=None, stream=None, want_state=True):
+    """Forward of one chunk that keeps its per-block products for
+    gdn_chunk_bwd_saved. Returns (o, S_out, saved)."""
+    lib = load()
+    s = shape_of(q, v)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+    if S_out is None and want_state:
+        S_out = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+    if saved is None:
+        saved = alloc_workspace(lib.gdn_chunk_saved_bytes(ctypes.byref(s)), q.device)
+    if workspace is None:
+        workspace = alloc_workspace(lib.gdn_chunk_workspace_bytes(ctypes.byref(s), GDN_WS_SAVED),
+                                    q.device)
+    rc = lib.gdn_chunk_fwd_save(ctypes.byref(s), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(S_in),
+                                _p(o), _p(S_out), _p(saved), saved.numel(), _p(workspace),
+                                workspace.numel(), _stream(stream))
+    _check(rc, "gdn_chunk_fwd_save")
+    return o, S_out, saved
+
+
+def gdn_chunk_bwd_saved(q, k, v, g, beta, S_in, dout, saved, dS_out=None, grads=None,
+                        dS_in=None, workspace=None, stream=None, want_state=True):
+    """Backward of one chunk from the products gdn_chunk_fwd_save kept.
+    Returns (dq, dk, dv, dg, dbeta, dS_in)."""
+    lib = load()
+    s = shape_of(q, v)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                 torch.empty_like(g), torch.empty_like(beta))
+    if dS_in is None and want_state:
+        dS_in = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(lib.gdn_chunk_workspace_bytes(ctypes.byref(s), GDN_WS_SAVED),
+                                    q.device)
+    rc = lib.gdn_chunk_bwd_saved(ctypes.byref(s), _p(q), _p(k), _p(v), _p(g), _p(beta),
+                                 _p(S_in), _p(dout), _p(dS_out), *[_p(t) for t in grads],
+                                 _p(dS_in), _p(saved), saved.numel(), _p(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(rc, "gdn_chunk_bwd_saved")
     return (*grads, dS_in)
 
 

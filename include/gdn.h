@@ -91,8 +91,10 @@ typedef struct {
   int dtype; /* gdn_dtype */
 } gdn_shape;
 
-/* Workspace bytes needed by gdn_chunk_fwd (is_bwd = 0) or gdn_chunk_bwd
- * (is_bwd = 1) for `shape`; 0 if the shape is invalid or unsupported. */
+/* Workspace bytes needed by gdn_chunk_fwd (is_bwd = 0), gdn_chunk_bwd
+ * (is_bwd = 1), or gdn_chunk_fwd_save / gdn_chunk_bwd_saved (is_bwd =
+ * GDN_WS_SAVED) for `shape`; 0 if the shape is invalid or unsupported. */
+#define GDN_WS_SAVED 2
 size_t gdn_chunk_workspace_bytes(const gdn_shape* shape, int is_bwd);
 
 /* Forward of one chunk (Eq. 5 chain: pass S_out as the next chunk's S_in).
@@ -109,6 +111,36 @@ gdn_status gdn_chunk_bwd(const gdn_shape* shape, const void* q, const void* k, c
                          const float* dS_out, void* dq, void* dk, void* dv, void* dg,
                          void* dbeta, float* dS_in, void* workspace, size_t workspace_bytes,
                          void* stream);
+
+/* Forward + backward that keep the forward's per-block products. The
+ * backward rebuilds the trajectory from S_in (Eq. 6); its first step is the
+ * same per-block Pre work (Eq. 2's decay cumsums, the masked K K^T / Q K^T,
+ * T = (I + A)^-1, W and U) that the forward already did on the same inputs.
+ * gdn_chunk_fwd_save computes exactly what gdn_chunk_fwd computes and also
+ * leaves those products (plus T and the masked K K^T the gradient needs) in
+ * `saved`; gdn_chunk_bwd_saved, given the same shape and inputs, reads them
+ * there instead of recomputing, and its results are bit-identical to
+ * gdn_chunk_bwd's. `saved` is a caller-owned device buffer of
+ * gdn_chunk_saved_bytes(shape) bytes, 256-byte aligned, that must not change
+ * between the two calls; `workspace` is gdn_chunk_workspace_bytes(shape,
+ * GDN_WS_SAVED) bytes (the same buffer can serve both calls). A null,
+ * misaligned or short `saved` returns GDN_ERR_WORKSPACE. Passing products of
+ * other inputs is not detected and gives the gradient of neither. For shapes
+ * on the fp32 kernels nothing is kept (gdn_chunk_saved_bytes returns 256)
+ * and the backward recomputes as gdn_chunk_bwd does. */
+size_t gdn_chunk_saved_bytes(const gdn_shape* shape);
+
+gdn_status gdn_chunk_fwd_save(const gdn_shape* shape, const void* q, const void* k,
+                              const void* v, const void* g, const void* beta, const float* S_in,
+                              void* o, float* S_out, void* saved, size_t saved_bytes,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+gdn_status gdn_chunk_bwd_saved(const gdn_shape* shape, const void* q, const void* k,
+                               const void* v, const void* g, const void* beta,
+                               const float* S_in, const void* dout, const float* dS_out,
+                               void* dq, void* dk, void* dv, void* dg, void* dbeta, float* dS_in,
+                               const void* saved, size_t saved_bytes, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /* Varlen (packed) variants: B must be 1 and T is the total token count.
  * cu_seqlens is a DEVICE int32 array of nseq + 1 offsets with cu[0] = 0,

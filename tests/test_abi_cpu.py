@@ -114,3 +114,30 @@ def test_varlen_host_checks(lib):
     assert lib.gdn_varlen_fwd(ctypes.byref(s), ctypes.c_void_p(FAKE), 0, *args) == 1  # nseq 0
     s2 = shape(B=2, T=300)
     assert lib.gdn_varlen_fwd(ctypes.byref(s2), ctypes.c_void_p(FAKE), 3, *args) == 1  # B != 1
+
+
+def test_saved_products_sizes_and_checks(lib):
+    s = shape()
+    saved = lib.gdn_chunk_saved_bytes(ctypes.byref(s))
+    ws_saved = lib.gdn_chunk_workspace_bytes(ctypes.byref(s), gdn.GDN_WS_SAVED)
+    ws_bwd = lib.gdn_chunk_workspace_bytes(ctypes.byref(s), 1)
+    assert saved > 0 and saved % 256 == 0
+    assert 0 < ws_saved < ws_bwd
+    assert lib.gdn_chunk_saved_bytes(ctypes.byref(shape(dk=64, dv=64, dtype=0))) == 256
+    assert lib.gdn_chunk_saved_bytes(ctypes.byref(shape(dk=96))) == 0
+    P = ctypes.c_void_p
+    fwd_args = [P(FAKE)] * 5 + [None, P(FAKE), None]
+
+    def fwd_save(sv, svb):
+        return lib.gdn_chunk_fwd_save(ctypes.byref(s), *fwd_args, sv, svb, P(FAKE),
+                                      ctypes.c_size_t(1 << 40), None)
+
+    assert fwd_save(None, 1 << 40) == 3                 # no saved buffer
+    assert fwd_save(P(FAKE + 16), 1 << 40) == 3         # misaligned
+    assert fwd_save(P(FAKE), saved - 256) == 3          # too small
+    bwd_args = [P(FAKE)] * 5 + [None, P(FAKE), None] + [P(FAKE)] * 5 + [None]
+    rc = lib.gdn_chunk_bwd_saved(ctypes.byref(s), *bwd_args, P(FAKE), saved, P(FAKE),
+                                 ws_saved - 256, None)
+    assert rc == 3                                      # workspace too small
+    rc = lib.gdn_chunk_bwd_saved(ctypes.byref(s), *bwd_args, None, saved, P(FAKE), ws_saved, None)
+    assert rc == 3
