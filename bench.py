@@ -106,6 +106,17 @@ def kernel_model(name, dk, dv, esz=2, C=64):
     elif name == "tc_chain_fwd":
         by = C * (3 * dk + dv) * esz + C * C * esz + C * f4 + C * dv * esz
         fl = 6 * C * dk * dv + 2 * C * C * dv
+    elif name == "tc_chain_fwd_keep":  # forward chain that also keeps H_b, V^new
+        by = (C * (3 * dk + dv) * esz + C * C * esz + C * f4 + C * dv * esz
+              + dk * dv * esz + C * dv * esz)
+        fl = 6 * C * dk * dv + 2 * C * C * dv
+    elif name == "tc_chain_rev":  # reverse chain alone
+        by = C * (3 * dk + dv) * esz + C * C * esz + C * f4 + dk * dv * esz + C * dv * esz
+        fl = 6 * C * dk * dv + 2 * C * C * dv
+    elif name == "tc_chains_bwd":  # recompute + reverse chains in one launch
+        by = (C * (2 * dk + dv) * esz + C * f4 + dk * dv * esz + C * dv * esz
+              + C * (3 * dk + dv) * esz + C * C * esz + C * f4 + dk * dv * esz + C * dv * esz)
+        fl = 4 * C * dk * dv + 6 * C * dk * dv + 2 * C * C * dv
     elif name == "tc_chain_recompute":
         by = C * (2 * dk + dv) * esz + C * f4 + dk * dv * esz + C * dv * esz
         fl = 4 * C * dk * dv

@@ -189,16 +189,24 @@ void carve_pre(const Plan& p, bool bwd, Carve& c, TcWs* ws, char* base) {
   }
 }
 
-// Bytes of the saved forward products (gdn_chunk_fwd_save / gdn_chunk_bwd_saved).
+// Bytes of the saved forward products (gdn_chunk_fwd_save / gdn_chunk_bwd_saved):
+// the Pre products with T and K K^T, and the chain's H_b and V^new per block.
 size_t saved_layout(const Plan& p, TcWs* ws, char* base) {
   Carve c;
   carve_pre(p, true, c, ws, base);
+  const size_t nbh = (size_t)p.nblk_cap * p.H;
+  const size_t o_Hb = c.take(2 * nbh * p.dv * p.dk);
+  const size_t o_Vn = c.take(2 * nbh * p.dv * BT);
+  if (base) {
+    ws->HbT = (__nv_bfloat16*)(base + o_Hb);
+    ws->VnT = (__nv_bfloat16*)(base + o_Vn);
+  }
   return c.off;
 }
 
 // Workspace layout of the tensor-core kernels. The first 256 bytes hold the
-// status word. WS_FWD / WS_BWD hold the Pre products themselves; WS_SAVED
-// leaves them to a separate saved-products buffer.
+// status word. WS_FWD / WS_BWD hold the Pre products themselves (WS_BWD also
+// H_b and V^new); WS_SAVED leaves those to a separate saved-products buffer.
 enum WsKind { WS_FWD = 0, WS_BWD = 1, WS_SAVED = 2 };
 size_t tc_layout(const Plan& p, int kind, TcWs* ws, int** blk0, int** blk_seq, char* base) {
   Carve c;
@@ -216,18 +224,21 @@ size_t tc_layout(const Plan& p, int kind, TcWs* ws, int** blk0, int** blk_seq, c
       carve_pre(p, bwd, pb, ws, base + o_pre);
     }
   }
+  const bool states = kind == WS_BWD;  // WS_SAVED: H_b, V^new live with the saved products
   size_t o_Hb = 0, o_Vn = 0, o_dH = 0, o_dVn = 0;
-  if (bwd) {
+  if (states) {
     o_Hb = c.take(2 * nbh * p.dv * p.dk);
     o_Vn = c.take(2 * nbh * p.dv * BT);
+  }
+  if (bwd) {
     o_dH = c.take(2 * nbh * p.dv * p.dk);
     o_dVn = c.take(2 * nbh * p.dv * BT);
   }
   if (base) {
     using bf = __nv_bfloat16;
     ws->status = (int*)(base + o_status);
-    ws->HbT = bwd ? (bf*)(base + o_Hb) : nullptr;
-    ws->VnT = bwd ? (bf*)(base + o_Vn) : nullptr;
+    ws->HbT = states ? (bf*)(base + o_Hb) : nullptr;
+    ws->VnT = states ? (bf*)(base + o_Vn) : nullptr;
     ws->dHT = bwd ? (bf*)(base + o_dH) : nullptr;
     ws->dVnT = bwd ? (bf*)(base + o_dVn) : nullptr;
     *blk0 = p.varlen ? (int*)(base + o_blk0) : nullptr;
@@ -298,8 +309,8 @@ gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, c
     TcWs w;
     tc_layout(p, kind, &w, &blk0, &blk_seq, (char*)ws);
     if (saved) {
-      saved_layout(p, &w, (char*)saved);
-      w.HbT = w.VnT = w.dHT = w.dVnT = nullptr;
+      saved_layout(p, &w, (char*)saved);  // the forward chain then also keeps H_b, V^new
+      w.dHT = w.dVnT = nullptr;
     }
     if (p.varlen && (e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st)))
       return GDN_ERR_CUDA;

@@ -79,6 +79,9 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
   const SeqInfo si = seq_info(m, s);
   FwdSmem<MODE, RG>& sm = *reinterpret_cast<FwdSmem<MODE, RG>*>(smraw);
   volatile int* abort = &sm.abort;
+  // H_b and V^new of every block go to the workspace for the gradient kernel:
+  // always when recomputing, and from the forward when the caller keeps them
+  const bool keep = MODE == CHAIN_RECOMPUTE || ws.HbT != nullptr;
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -156,7 +159,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
       const int tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
       const size_t bh = (size_t)(si.blk0 + lb) * H + h;
       const float* dec = S.dec;
-      if (MODE == CHAIN_RECOMPUTE && ok) {
+      if (keep && ok) {
         __nv_bfloat16* Hg = ws.HbT + bh * DV * DK + (size_t)tile * BV * DK;
         for (int idx = tid; idx < BV * 16; idx += 128) {
           const int r = idx >> 4, c = (idx & 15) * 8;
@@ -223,7 +226,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
             *reinterpret_cast<uint32_t*>(&sm.VnT[vr * LD64 + t0]) = pv;
             *reinterpret_cast<uint32_t*>(&sm.VsT[vr * LD64 + t0]) =
                 pack_bf16(v0 * dec[BT + t0], v1 * dec[BT + t0 + 1]);
-            if (MODE == CHAIN_RECOMPUTE && ok)
+            if (keep && ok)
               *reinterpret_cast<uint32_t*>(ws.VnT + bh * DV * BT + (size_t)(tile * BV + vr) * BT + t0) = pv;
           }
       // operands of the state update that do not depend on V^new: load before the barrier
@@ -622,6 +625,18 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     chain_rev_body<DV, BWD_RG>(m, blockIdx.x - n, q, k, dout, dS_out, dS_in, ws, smraw);
 }
 
+// Backward from kept forward products: H_b and V^new are already in the
+// workspace, so only the reverse chain runs, 16 value columns per CTA.
+template <int DV>
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+    k_chain_rev(SeqMap m, const __nv_bfloat16* __restrict__ q,
+                const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ dout,
+                const float* dS_out, float* dS_in, TcWs ws) {
+  extern __shared__ __align__(128) unsigned char smraw[];
+  if (m.cu == nullptr && blockIdx.x == 0 && threadIdx.x == 0) ws.status[0] = DEV_OK;
+  chain_rev_body<DV, 1>(m, blockIdx.x, q, k, dout, dS_out, dS_in, ws, smraw);
+}
+
 template <class K>
 cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -636,7 +651,7 @@ cudaError_t fwd_t(const SeqMap& m, const void* q, const void* k, const void* v, 
   if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, st))) return e;
   constexpr size_t smem = sizeof(FwdSmem<CHAIN_FWD, 1>);
   if ((e = set_smem(k_chain_fwd<DV>, smem))) return e;
-  prof_mark(st, "tc_chain_fwd");
+  prof_mark(st, ws.HbT ? "tc_chain_fwd_keep" : "tc_chain_fwd");
   k_chain_fwd<DV><<<m.nseq * m.H * (DV / 16), CHAIN_THREADS, smem, st>>>(
       m, (const bf*)q, (const bf*)k, S_in, S_out, (bf*)o, ws);
   prof_mark(st, nullptr);
@@ -650,7 +665,19 @@ cudaError_t bwd_t(const SeqMap& m, const void* q, const void* k, const void* v, 
                   const TcWs& ws, bool run_pre, cudaStream_t st) {
   using bf = __nv_bfloat16;
   cudaError_t e;
-  if (run_pre && (e = tc_pre(m, DV, q, k, v, g, beta, ws, st))) return e;
+  if (!run_pre) {
+    // H_b, V^new and the Pre products come from the forward call
+    constexpr size_t smem = sizeof(RevSmem<1>);
+    if ((e = set_smem(k_chain_rev<DV>, smem))) return e;
+    prof_mark(st, "tc_chain_rev");
+    k_chain_rev<DV><<<m.nseq * m.H * (DV / 16), CHAIN_THREADS, smem, st>>>(
+        m, (const bf*)q, (const bf*)k, (const bf*)dout, dS_out, dS_in, ws);
+    if ((e = cudaGetLastError())) return e;
+    if ((e = tc_grad(m, DV, q, k, v, beta, dout, dq, dkk, dvv, dg, dbeta, ws, st))) return e;
+    prof_mark(st, nullptr);
+    return cudaGetLastError();
+  }
+  if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, st))) return e;
   constexpr size_t s1 = sizeof(FwdSmem<CHAIN_RECOMPUTE, BWD_RG>);
   constexpr size_t s2 = sizeof(RevSmem<BWD_RG>);
   constexpr size_t smem = s1 > s2 ? s1 : s2;

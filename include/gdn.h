@@ -117,10 +117,11 @@ gdn_status gdn_chunk_bwd(const gdn_shape* shape, const void* q, const void* k, c
  * same per-block Pre work (Eq. 2's decay cumsums, the masked K K^T / Q K^T,
  * T = (I + A)^-1, W and U) that the forward already did on the same inputs.
  * gdn_chunk_fwd_save computes exactly what gdn_chunk_fwd computes and also
- * leaves those products (plus T and the masked K K^T the gradient needs) in
- * `saved`; gdn_chunk_bwd_saved, given the same shape and inputs, reads them
- * there instead of recomputing, and its results are bit-identical to
- * gdn_chunk_bwd's. `saved` is a caller-owned device buffer of
+ * leaves those products (plus T and the masked K K^T the gradient needs) and
+ * the chain's per-block state H_b and V^new (bf16) in `saved`;
+ * gdn_chunk_bwd_saved, given the same shape and inputs, reads them there
+ * instead of recomputing them (only the reverse chain and the gradient kernel
+ * run), and its results are bit-identical to gdn_chunk_bwd's. `saved` is a caller-owned device buffer of
  * gdn_chunk_saved_bytes(shape) bytes, 256-byte aligned, that must not change
  * between the two calls; `workspace` is gdn_chunk_workspace_bytes(shape,
  * GDN_WS_SAVED) bytes (the same buffer can serve both calls). A null,
