@@ -169,7 +169,7 @@ size_t simt_layout(const Plan& p, bool bwd, SimtWs* ws, int** blk0, int** blk_se
 void carve_pre(const Plan& p, bool bwd, Carve& c, TcWs* ws, char* base) {
   using bf = __nv_bfloat16;
   const size_t nbh = (size_t)p.nblk_cap * p.H;
-  const size_t o_dec = c.take(4 * nbh * 3 * BT);
+  const size_t o_dec = c.take(4 * nbh * TC_DEC_ROWS * BT);
   const size_t o_W = c.take(2 * nbh * BT * TC_LDK);
   const size_t o_U = c.take(2 * nbh * (p.dv / 16) * BT * TC_LDU);
   const size_t o_QKM = c.take(2 * nbh * BT * TC_LD64);

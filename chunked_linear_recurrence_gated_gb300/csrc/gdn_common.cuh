@@ -89,9 +89,11 @@ struct SimtWs {
 constexpr int TC_LDK = 136;   // padded row of 128-wide bf16 tiles
 constexpr int TC_LD64 = 72;   // padded row of 64-wide bf16 tiles
 constexpr int TC_LDU = 24;    // padded row of a 16-column U tile
+constexpr int TC_DEC_ROWS = 4;  // per-block vectors in TcWs::dec
 struct TcWs {
   int* status;
-  float* dec;            // [nblk, H, 3, BT]   Gamma_r, e^{gamma_C - gamma_r}, gamma_r
+  float* dec;            // [nblk, H, 4, BT]   Gamma_r, e^{gamma_C - gamma_r}, gamma_r, beta_r
+                         //                    (beta_r = 0 past the end of the block)
   __nv_bfloat16* W;      // [nblk, H, BT, TC_LDK]          W = T diag(beta Gamma) K
   __nv_bfloat16* U;      // [nblk, H, dv/16, BT, TC_LDU]   U = T diag(beta) V, tile-major
   __nv_bfloat16* QKM;    // [nblk, H, BT, TC_LD64]         Q K^T * Mask (j <= r)

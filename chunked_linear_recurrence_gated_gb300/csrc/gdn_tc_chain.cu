@@ -133,7 +133,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
         mbar_arrive_expect_tx(fb, bytes);
         bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, fb);
         bulk_g2s(S.K, ws.Kp + bh * BT * LDK, BT * LDK * 2, fb);
-        bulk_g2s(S.dec, ws.dec + bh * 3 * BT, 3 * BT * 4, fb);
+        bulk_g2s(S.dec, ws.dec + bh * TC_DEC_ROWS * BT, 3 * BT * 4, fb);
         bulk_g2s(S.U, ws.U + (bh * (DV / 16) + (size_t)tile * RG) * BT * LDU, RG * BT * LDU * 2, fb);
         if (MODE == CHAIN_FWD) {
           bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, BT * LDK * 2, fb);
@@ -425,7 +425,7 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
         bulk_g2s(S.K, ws.Kp + bh * BT * LDK, BT * LDK * 2, fb);
         bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, BT * LDK * 2, fb);
         bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, fb);
-        bulk_g2s(S.dec, ws.dec + bh * 3 * BT, 3 * BT * 4, fb);
+        bulk_g2s(S.dec, ws.dec + bh * TC_DEC_ROWS * BT, 3 * BT * 4, fb);
       }
       // the dO tile: 16-byte cp.async per lane, rows past the block's end zero-filled
 #pragma unroll

@@ -34,21 +34,25 @@ struct GradLate {                 // used only after the value-dimension loop
   __nv_bfloat16 X[BT * LD64];     // dT, later Z1 = T^T dT
 };
 
-struct GradSmem {
+struct GradBlk {                  // one block-head's operands (double-buffered across blocks)
   __nv_bfloat16 Q[BT * LDK];
   __nv_bfloat16 K[BT * LDK];
   __nv_bfloat16 T[BT * LD64];
-  union {
-    GradChunk ch[2];              // double-buffered value chunks
-    GradLate late;
-  } u;
-  float g[BT], b[BT], G[BT], dte[BT];
+  __nv_bfloat16 QKM[BT * LD64];   // Pre's Q K^T * Mask
+  __nv_bfloat16 KKM[BT * LD64];   // Pre's K K^T * Mask
+  float dec[TC_DEC_ROWS * BT];    // Gamma, e^{gamma_C - gamma}, gamma, beta
+};
+
+struct GradSmem {
+  GradBlk blk[2];
+  GradChunk ch[2];  // double-buffered value chunks; ch[1] doubles as GradLate after the loop
   float rowacc[2][BT];   // per column half
   float colacc[4][BT];   // per row quarter
   float dbeta[2][BT];
   float rho[2][BT];
   float red[8];
 };
+static_assert(sizeof(GradLate) <= sizeof(GradChunk), "late tiles overlay one chunk buffer");
 
 __device__ __forceinline__ float quad_reduce(float x) {
   x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -63,11 +67,13 @@ __device__ __forceinline__ float col_reduce(float x) {
   return x;
 }
 
+// Persistent: each CTA walks block-heads it = blockIdx.x, + gridDim.x, ...
+// While one block-head's last value chunk and its late phases run, the next
+// one's operands and first value chunk are already in flight.
 template <int DV>
 __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat16* __restrict__ q,
                                                     const __nv_bfloat16* __restrict__ k,
                                                     const __nv_bfloat16* __restrict__ v,
-                                                    const __nv_bfloat16* __restrict__ beta,
                                                     const __nv_bfloat16* __restrict__ dout,
                                                     __nv_bfloat16* __restrict__ dq,
                                                     __nv_bfloat16* __restrict__ dk,
@@ -75,62 +81,51 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
                                                     __nv_bfloat16* __restrict__ dg,
                                                     __nv_bfloat16* __restrict__ dbeta, TcWs ws) {
   constexpr int DK = 128;
-  BlockInfo bi;
-  const int gb = blockIdx.x, h = blockIdx.y, H = m.H, tid = threadIdx.x;
-  if (!block_info(m, gb, bi)) return;
+  constexpr int NCH = DV / VC;
+  static_assert(NCH % 2 == 0, "the last chunk must use buffer 1");
+  const int H = m.H, tid = threadIdx.x;
+  const int total = m.nblk_cap * H;
   extern __shared__ __align__(128) unsigned char smraw[];
   GradSmem& sm = *reinterpret_cast<GradSmem*>(smraw);
+  GradLate& late = *reinterpret_cast<GradLate*>(&sm.ch[1]);
   const int w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
   const int rw = w & 3, cw = w >> 2;
   const int R0 = 16 * rw;
-  const size_t bh = (size_t)gb * H + h;
 
-  for (int idx = tid; idx < BT * 16; idx += 256) {
-    const int r = idx >> 4, c = (idx & 15) * 8;
-    const bool ok = r < bi.len;
-    const size_t off = ((size_t)(bi.tok0 + (ok ? r : 0)) * H + h) * DK + c;
-    cp16(&sm.Q[r * LDK + c], q + off, ok);
-    cp16(&sm.K[r * LDK + c], k + off, ok);
-  }
-  for (int idx = tid; idx < BT * 8; idx += 256) {
-    const int r = idx >> 3, c = (idx & 7) * 8;
-    cp16(&sm.T[r * LD64 + c], ws.T + bh * BT * BT + r * BT + c, true);
-  }
-  if (tid < BT) {
-    const bool ok = tid < bi.len;
-    const float* dec = ws.dec + bh * 3 * BT;
-    sm.G[tid] = dec[tid];
-    sm.dte[tid] = dec[BT + tid];
-    sm.g[tid] = dec[2 * BT + tid];
-    sm.b[tid] = ok ? __bfloat162float(beta[(size_t)(bi.tok0 + tid) * H + h]) : 0.f;
-  }
-  for (int idx = tid; idx < 2 * BT; idx += 256) {
-    (&sm.rowacc[0][0])[idx] = 0.f;
-    (&sm.dbeta[0][0])[idx] = 0.f;
-    (&sm.rho[0][0])[idx] = 0.f;
-  }
-  for (int idx = tid; idx < 4 * BT; idx += 256) (&sm.colacc[0][0])[idx] = 0.f;
-  __syncthreads();
-
-  // ---- value-dimension reductions
-  float aOH[8][4], aHW[8][4], aKt[8][4], aOV[4][4], aWV[4][4];
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) aOH[j][e] = aHW[j][e] = aKt[j][e] = 0.f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) aOV[j][e] = aWV[j][e] = 0.f;
-  float hd = 0.f, ybeta = 0.f;
-
-  auto load_chunk = [&](int c) {
-    GradChunk& C = sm.u.ch[c & 1];
+  auto next_valid = [&](int it, BlockInfo& b) {
+    while (it < total && !block_info(m, it / H, b)) it += gridDim.x;
+    return it;
+  };
+  // operands of block-head `it` into blk[buf] (no commit)
+  auto load_blk = [&](int it, const BlockInfo& b, int buf) {
+    GradBlk& B = sm.blk[buf];
+    const int h = it % H;
+    const size_t bh = (size_t)it;
+    for (int idx = tid; idx < BT * 16; idx += 256) {
+      const int r = idx >> 4, c = (idx & 15) * 8;
+      const bool ok = r < b.len;
+      const size_t off = ((size_t)(b.tok0 + (ok ? r : 0)) * H + h) * DK + c;
+      cp16(&B.Q[r * LDK + c], q + off, ok);
+      cp16(&B.K[r * LDK + c], k + off, ok);
+    }
+    for (int idx = tid; idx < BT * 8; idx += 256) {
+      const int r = idx >> 3, c = (idx & 7) * 8;
+      cp16(&B.T[r * LD64 + c], ws.T + bh * BT * BT + r * BT + c, true);
+      cp16(&B.QKM[r * LD64 + c], ws.QKM + bh * BT * LD64 + r * LD64 + c, true);
+      cp16(&B.KKM[r * LD64 + c], ws.KKM + bh * BT * LD64 + r * LD64 + c, true);
+    }
+    if (tid < TC_DEC_ROWS * BT / 4) cp16(&B.dec[4 * tid], ws.dec + bh * TC_DEC_ROWS * BT + 4 * tid, true);
+  };
+  // value chunk c of block-head `it` into ch[c & 1] (no commit)
+  auto load_chunk = [&](int it, const BlockInfo& b, int c) {
+    GradChunk& C = sm.ch[c & 1];
+    const int h = it % H;
+    const size_t bh = (size_t)it;
     const int v0 = c * VC;
     for (int idx = tid; idx < BT * (VC / 8); idx += 256) {
       const int r = idx / (VC / 8), cc = (idx % (VC / 8)) * 8;
-      const bool ok = r < bi.len;
-      const size_t tok = (size_t)(bi.tok0 + (ok ? r : 0)) * H + h;
+      const bool ok = r < b.len;
+      const size_t tok = (size_t)(b.tok0 + (ok ? r : 0)) * H + h;
       cp16(&C.dO[r * LDC + cc], dout + tok * DV + v0 + cc, ok);
       cp16(&C.V[r * LDC + cc], v + tok * DV + v0 + cc, ok);
     }
@@ -145,19 +140,55 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       cp16(&C.dHT[r * LDK + cc], ws.dHT + bh * DV * DK + (size_t)(v0 + r) * DK + cc, true);
     }
   };
-  constexpr int NCH = DV / VC;
-  load_chunk(0);
+
+  BlockInfo bi;
+  int it = next_valid(blockIdx.x, bi);
+  int buf = 0;
+  if (it < total) {
+    load_blk(it, bi, buf);
+    load_chunk(it, bi, 0);
+  }
   cp_commit();
+  for (; it < total; buf ^= 1) {
+  BlockInfo nbi;
+  const int nit = next_valid(it + gridDim.x, nbi);
+  const int h = it % H;
+  const GradBlk& Bk = sm.blk[buf];
+  const float* sG = Bk.dec;
+  const float* sdte = Bk.dec + BT;
+  const float* sg = Bk.dec + 2 * BT;
+  const float* sb = Bk.dec + 3 * BT;
+  for (int idx = tid; idx < 2 * BT; idx += 256) {
+    (&sm.rowacc[0][0])[idx] = 0.f;
+    (&sm.dbeta[0][0])[idx] = 0.f;
+    (&sm.rho[0][0])[idx] = 0.f;
+  }
+  for (int idx = tid; idx < 4 * BT; idx += 256) (&sm.colacc[0][0])[idx] = 0.f;
+
+  // ---- value-dimension reductions
+  float aOH[8][4], aHW[8][4], aKt[8][4], aOV[4][4], aWV[4][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) aOH[j][e] = aHW[j][e] = aKt[j][e] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) aOV[j][e] = aWV[j][e] = 0.f;
+  float hd = 0.f, ybeta = 0.f;
+
   for (int c = 0; c < NCH; ++c) {
     if (c + 1 < NCH) {
-      load_chunk(c + 1);
-      cp_commit();
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
+      load_chunk(it, bi, c + 1);
+    } else if (nit < total) {
+      // the last chunk computes from ch[1]: ch[0] and the other operand buffer are free
+      load_blk(nit, nbi, buf ^ 1);
+      load_chunk(nit, nbi, 0);
     }
+    cp_commit();
+    cp_wait<1>();
     __syncthreads();
-    const GradChunk& C = sm.u.ch[c & 1];
+    const GradChunk& C = sm.ch[c & 1];
 #pragma unroll
     for (int kc = 0; kc < VC / 16; ++kc) {
       uint32_t aO[4], aW[4], aV[4], bH[4][4], bD[4][4], bN[2][4], bVv[2][4];
@@ -214,7 +245,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       uint32_t at_[4][4], bY[4][4];
 #pragma unroll
       for (int kc = 0; kc < 4; ++kc) {
-        lda_tr(at_[kc], sm.T, LD64, R0, 16 * kc);
+        lda_tr(at_[kc], Bk.T, LD64, R0, 16 * kc);
         ldb_nk_x2n(bY[kc], C.dVnT, LD64, 16 * cw, 16 * kc);
       }
 #pragma unroll
@@ -232,7 +263,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
           const float y0 = y[j][2 * hf], y1 = y[j][2 * hf + 1];
           if (r < bi.len)
             *reinterpret_cast<uint32_t*>(dvo + ((size_t)(bi.tok0 + r) * H + h) * DV + c * VC + cc) =
-                pack_bf16(sm.b[r] * y0, sm.b[r] * y1);
+                pack_bf16(sb[r] * y0, sb[r] * y1);
           const float yv = y0 * vv.x + y1 * vv.y;
           if (hf == 0) p0 += yv; else p1 += yv;
         }
@@ -260,10 +291,10 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = R0 + gq + 8 * (e >> 1), c = 64 * cw + 8 * j + 2 * tq + (e & 1);
-        const float qv = __bfloat162float(sm.Q[r * LDK + c]);
-        const float kv = __bfloat162float(sm.K[r * LDK + c]);
-        aQ[j][e] = sm.G[r] * aOH[j][e];
-        aK[j][e] = sm.dte[r] * aKt[j][e];
+        const float qv = __bfloat162float(Bk.Q[r * LDK + c]);
+        const float kv = __bfloat162float(Bk.K[r * LDK + c]);
+        aQ[j][e] = sG[r] * aOH[j][e];
+        aK[j][e] = sdte[r] * aKt[j][e];
         if (e < 2) {
           pq0 += qv * aOH[j][e];
           pk0 += kv * aKt[j][e];
@@ -278,10 +309,10 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
     pk1 = quad_reduce(pk1);
     if (tq == 0) {
       const int r0 = R0 + gq, r1 = R0 + gq + 8;
-      sm.rowacc[cw][r0] += sm.G[r0] * pq0;
-      sm.rowacc[cw][r1] += sm.G[r1] * pq1;
-      sm.rho[cw][r0] = sm.dte[r0] * pk0;
-      sm.rho[cw][r1] = sm.dte[r1] * pk1;
+      sm.rowacc[cw][r0] += sG[r0] * pq0;
+      sm.rowacc[cw][r1] += sG[r1] * pq1;
+      sm.rho[cw][r0] = sdte[r0] * pk0;
+      sm.rho[cw][r1] = sdte[r1] * pk1;
     }
     // HW -> smem (bf16)
 #pragma unroll
@@ -289,15 +320,15 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int r = R0 + gq + 8 * hf, c = 64 * cw + 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(&sm.u.late.HW[r * LDK + c]) = pack_bf16(aHW[j][2 * hf], aHW[j][2 * hf + 1]);
+        *reinterpret_cast<uint32_t*>(&late.HW[r * LDK + c]) = pack_bf16(aHW[j][2 * hf], aHW[j][2 * hf + 1]);
       }
   }
   // ---- P = dOV * Mask -> smem ; R = P * (Q K^T) = dOV * QKM (Pre's masked Q K^T)
   //      -> row / column sums ; partial dT = beta_c dWV ; K K^T * Mask for the dA step
   float dT[4][4], kk[4][4];
   {
-    const __nv_bfloat16* qkm = ws.QKM + bh * BT * LD64;
-    const __nv_bfloat16* kkm = ws.KKM + bh * BT * LD64;
+    const __nv_bfloat16* qkm = Bk.QKM;
+    const __nv_bfloat16* kkm = Bk.KKM;
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -309,18 +340,18 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
         const float2 km = unpack_bf16(*reinterpret_cast<const uint32_t*>(kkm + r * LD64 + c));
         kk[j][2 * hf] = km.x;
         kk[j][2 * hf + 1] = km.y;
-        const float m0 = (c <= r) ? __expf(sm.g[r] - sm.g[c]) : 0.f;
-        const float m1 = (c + 1 <= r) ? __expf(sm.g[r] - sm.g[c + 1]) : 0.f;
+        const float m0 = (c <= r) ? __expf(sg[r] - sg[c]) : 0.f;
+        const float m1 = (c + 1 <= r) ? __expf(sg[r] - sg[c + 1]) : 0.f;
         const float R0v = aOV[j][2 * hf] * qm.x, R1v = aOV[j][2 * hf + 1] * qm.y;
         if (hf == 0) rs0 += R0v + R1v; else rs1 += R0v + R1v;
         cs0 += R0v;
         cs1 += R1v;
         aOV[j][2 * hf] *= m0;  // P in fp32
         aOV[j][2 * hf + 1] *= m1;
-        *reinterpret_cast<uint32_t*>(&sm.u.late.P[r * LD64 + c]) =
+        *reinterpret_cast<uint32_t*>(&late.P[r * LD64 + c]) =
             pack_bf16(aOV[j][2 * hf], aOV[j][2 * hf + 1]);
-        dT[j][2 * hf] = sm.b[c] * aWV[j][2 * hf];
-        dT[j][2 * hf + 1] = sm.b[c + 1] * aWV[j][2 * hf + 1];
+        dT[j][2 * hf] = sb[c] * aWV[j][2 * hf];
+        dT[j][2 * hf + 1] = sb[c + 1] * aWV[j][2 * hf + 1];
       }
       cs0 = col_reduce(cs0);
       cs1 = col_reduce(cs1);
@@ -348,9 +379,9 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
     for (int kc = 0; kc < DK / 16; ++kc) {
       uint32_t ah_[4], b0[4], b1[4];
-      lda_rm(ah_, sm.u.late.HW, LDK, R0, 16 * kc);
-      ldb_nk_x2n(b0, sm.K, LDK, 32 * cw, 16 * kc);
-      ldb_nk_x2n(b1, sm.K, LDK, 32 * cw + 16, 16 * kc);
+      lda_rm(ah_, late.HW, LDK, R0, 16 * kc);
+      ldb_nk_x2n(b0, Bk.K, LDK, 32 * cw, 16 * kc);
+      ldb_nk_x2n(b1, Bk.K, LDK, 32 * cw + 16, 16 * kc);
       mma16816(hk[0], ah_, b0[0], b0[1]);
       mma16816(hk[1], ah_, b0[2], b0[3]);
       mma16816(hk[2], ah_, b1[0], b1[1]);
@@ -361,14 +392,14 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c = 32 * cw + 8 * j + 2 * tq + (e & 1);
-        dT[j][e] -= sm.b[c] * sm.G[c] * hk[j][e];
+        dT[j][e] -= sb[c] * sG[c] * hk[j][e];
       }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int r = R0 + gq + 8 * hf, c = 32 * cw + 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(&sm.u.late.X[r * LD64 + c]) = pack_bf16(dT[j][2 * hf], dT[j][2 * hf + 1]);
+        *reinterpret_cast<uint32_t*>(&late.X[r * LD64 + c]) = pack_bf16(dT[j][2 * hf], dT[j][2 * hf + 1]);
       }
   }
   __syncthreads();
@@ -382,19 +413,19 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
     for (int kc = 0; kc < 4; ++kc) {
       uint32_t ap[4], apt[4], att[4];
-      lda_rm(ap, sm.u.late.P, LD64, R0, 16 * kc);
-      lda_tr(apt, sm.u.late.P, LD64, R0, 16 * kc);
-      lda_tr(att, sm.T, LD64, R0, 16 * kc);
+      lda_rm(ap, late.P, LD64, R0, 16 * kc);
+      lda_tr(apt, late.P, LD64, R0, 16 * kc);
+      lda_tr(att, Bk.T, LD64, R0, 16 * kc);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         uint32_t b[4];
-        ldb_kn_x2n(b, sm.K, LDK, 16 * kc, 64 * cw + 16 * jj);
+        ldb_kn_x2n(b, Bk.K, LDK, 16 * kc, 64 * cw + 16 * jj);
         mma16816(aQ[2 * jj], ap, b[0], b[1]);
         mma16816(aQ[2 * jj + 1], ap, b[2], b[3]);
-        ldb_kn_x2n(b, sm.Q, LDK, 16 * kc, 64 * cw + 16 * jj);
+        ldb_kn_x2n(b, Bk.Q, LDK, 16 * kc, 64 * cw + 16 * jj);
         mma16816(aK[2 * jj], apt, b[0], b[1]);
         mma16816(aK[2 * jj + 1], apt, b[2], b[3]);
-        ldb_kn_x2n(b, sm.u.late.HW, LDK, 16 * kc, 64 * cw + 16 * jj);
+        ldb_kn_x2n(b, late.HW, LDK, 16 * kc, 64 * cw + 16 * jj);
         mma16816(xg[2 * jj], att, b[0], b[1]);
         mma16816(xg[2 * jj + 1], att, b[2], b[3]);
       }
@@ -406,18 +437,18 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       for (int e = 0; e < 4; ++e) {
         const int r = R0 + gq + 8 * (e >> 1), c = 64 * cw + 8 * j + 2 * tq + (e & 1);
         const float x = -xg[j][e];
-        aK[j][e] += sm.b[r] * sm.G[r] * x;
-        const float kx = x * __bfloat162float(sm.K[r * LDK + c]);
+        aK[j][e] += sb[r] * sG[r] * x;
+        const float kx = x * __bfloat162float(Bk.K[r * LDK + c]);
         if (e < 2) p0 += kx; else p1 += kx;
       }
     p0 = quad_reduce(p0);
     p1 = quad_reduce(p1);
     if (tq == 0) {
       const int r0 = R0 + gq, r1 = R0 + gq + 8;
-      sm.dbeta[cw][r0] += sm.G[r0] * p0;
-      sm.dbeta[cw][r1] += sm.G[r1] * p1;
-      sm.rowacc[cw][r0] += sm.b[r0] * sm.G[r0] * p0;
-      sm.rowacc[cw][r1] += sm.b[r1] * sm.G[r1] * p1;
+      sm.dbeta[cw][r0] += sG[r0] * p0;
+      sm.dbeta[cw][r1] += sG[r1] * p1;
+      sm.rowacc[cw][r0] += sb[r0] * sG[r0] * p0;
+      sm.rowacc[cw][r1] += sb[r1] * sG[r1] * p1;
     }
   }
   float z1[4][4];
@@ -428,10 +459,10 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
   for (int kc = 0; kc < 4; ++kc) {
     uint32_t att[4], b[4];
-    lda_tr(att, sm.T, LD64, R0, 16 * kc);
+    lda_tr(att, Bk.T, LD64, R0, 16 * kc);
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
-      ldb_kn_x2n(b, sm.u.late.X, LD64, 16 * kc, 32 * cw + 16 * jj);
+      ldb_kn_x2n(b, late.X, LD64, 16 * kc, 32 * cw + 16 * jj);
       mma16816(z1[2 * jj], att, b[0], b[1]);
       mma16816(z1[2 * jj + 1], att, b[2], b[3]);
     }
@@ -442,7 +473,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
       const int r = R0 + gq + 8 * hf, c = 32 * cw + 8 * j + 2 * tq;
-      *reinterpret_cast<uint32_t*>(&sm.u.late.X[r * LD64 + c]) = pack_bf16(z1[j][2 * hf], z1[j][2 * hf + 1]);
+      *reinterpret_cast<uint32_t*>(&late.X[r * LD64 + c]) = pack_bf16(z1[j][2 * hf], z1[j][2 * hf + 1]);
     }
   __syncthreads();
   // ---- dA = strictly-lower(-Z1 T^T); E = dA * Mask; BE = diag(beta) E
@@ -455,10 +486,10 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
     for (int kc = 0; kc < 4; ++kc) {
       uint32_t a[4], b[4];
-      lda_rm(a, sm.u.late.X, LD64, R0, 16 * kc);
+      lda_rm(a, late.X, LD64, R0, 16 * kc);
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
-        ldb_nk_x2n(b, sm.T, LD64, 32 * cw + 16 * jj, 16 * kc);
+        ldb_nk_x2n(b, Bk.T, LD64, 32 * cw + 16 * jj, 16 * kc);
         mma16816(da[2 * jj], a, b[0], b[1]);
         mma16816(da[2 * jj + 1], a, b[2], b[3]);
       }
@@ -471,9 +502,9 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       for (int e = 0; e < 4; ++e) {
         const int r = R0 + gq + 8 * (e >> 1), c = 32 * cw + 8 * j + 2 * tq + (e & 1);
         const float dA = (c < r) ? -da[j][e] : 0.f;
-        const float E = (c < r) ? dA * __expf(sm.g[r] - sm.g[c]) : 0.f;
+        const float E = (c < r) ? dA * __expf(sg[r] - sg[c]) : 0.f;
         const float dAK = dA * kk[j][e];  // dA * K K^T * Mask = E * K K^T
-        const float Gv = sm.b[r] * dAK;
+        const float Gv = sb[r] * dAK;
         if (e < 2) {
           pb0 += dAK;
           rg0 += Gv;
@@ -482,7 +513,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
           rg1 += Gv;
         }
         if (e & 1) cg1 += Gv; else cg0 += Gv;
-        da[j][e] = sm.b[r] * E;
+        da[j][e] = sb[r] * E;
       }
       cg0 = col_reduce(cg0);
       cg1 = col_reduce(cg1);
@@ -508,7 +539,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int r = R0 + gq + 8 * hf, c = 32 * cw + 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(&sm.u.late.P[r * LD64 + c]) = pack_bf16(da[j][2 * hf], da[j][2 * hf + 1]);
+        *reinterpret_cast<uint32_t*>(&late.P[r * LD64 + c]) = pack_bf16(da[j][2 * hf], da[j][2 * hf + 1]);
       }
   }
   __syncthreads();
@@ -516,12 +547,12 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
   for (int kc = 0; kc < 4; ++kc) {
     uint32_t a[4], at_[4];
-    lda_rm(a, sm.u.late.P, LD64, R0, 16 * kc);
-    lda_tr(at_, sm.u.late.P, LD64, R0, 16 * kc);
+    lda_rm(a, late.P, LD64, R0, 16 * kc);
+    lda_tr(at_, late.P, LD64, R0, 16 * kc);
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       uint32_t b[4];
-      ldb_kn_x2n(b, sm.K, LDK, 16 * kc, 64 * cw + 16 * jj);
+      ldb_kn_x2n(b, Bk.K, LDK, 16 * kc, 64 * cw + 16 * jj);
       mma16816(aK[2 * jj], a, b[0], b[1]);
       mma16816(aK[2 * jj + 1], a, b[2], b[3]);
       mma16816(aK[2 * jj], at_, b[0], b[1]);
@@ -543,9 +574,11 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
   __syncthreads();
   if (tid < 32) {
     // dgamma_r = row terms - column terms - rho_r; the gamma_C terms land on the last row
-    float hs = 0.f, rho = 0.f;
+    float hs = 0.f;
     for (int i = 0; i < 8; ++i) hs += sm.red[i];
-    for (int i = 0; i < BT; ++i) rho += sm.rho[0][i] + sm.rho[1][i];
+    float rho = sm.rho[0][l] + sm.rho[1][l] + sm.rho[0][l + 32] + sm.rho[1][l + 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) rho += __shfl_xor_sync(0xffffffffu, rho, off);
     float dgam[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -553,7 +586,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       dgam[hh] = sm.rowacc[0][r] + sm.rowacc[1][r] - sm.colacc[0][r] - sm.colacc[1][r] -
                  sm.colacc[2][r] - sm.colacc[3][r] - sm.rho[0][r] - sm.rho[1][r];
     }
-    if (l == 31) dgam[1] += rho + sm.G[BT - 1] * hs;
+    if (l == 31) dgam[1] += rho + sG[BT - 1] * hs;
     // reverse inclusive cumsum over 64 rows (fixed order)
     float a = dgam[1], c = dgam[0];
 #pragma unroll
@@ -580,6 +613,11 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       dbeta[tok] = __float2bfloat16_rn(db1);
     }
   }
+  __syncthreads();  // vectors, the late tiles and this operand buffer are reused next
+  it = nit;
+  bi = nbi;
+  }
+  cp_wait<0>();
 }
 
 template <class K>
@@ -594,12 +632,18 @@ cudaError_t launch_grad(const SeqMap& m, const void* q, const void* k, const voi
   using bf = __nv_bfloat16;
   cudaError_t e;
   if ((e = set_smem(k_grad_tc<DV>, sizeof(GradSmem)))) return e;
-  if (m.nblk_cap > 0) {
+  const long long items = (long long)m.nblk_cap * m.H;
+  if (items > 0) {
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
+      return e;
+    const int grid = (int)(items < sms ? items : sms);  // one resident CTA per SM
     prof_mark(st, "tc_grad");
-    k_grad_tc<DV><<<dim3(m.nblk_cap, m.H), 256, sizeof(GradSmem), st>>>(
-        m, (const bf*)q, (const bf*)k, (const bf*)v, (const bf*)beta, (const bf*)dout, (bf*)dq,
-        (bf*)dkk, (bf*)dvv, (bf*)dg, (bf*)dbeta, ws);
+    k_grad_tc<DV><<<grid, 256, sizeof(GradSmem), st>>>(
+        m, (const bf*)q, (const bf*)k, (const bf*)v, (const bf*)dout, (bf*)dq, (bf*)dkk, (bf*)dvv,
+        (bf*)dg, (bf*)dbeta, ws);
   }
+  (void)beta;
   return cudaGetLastError();
 }
 

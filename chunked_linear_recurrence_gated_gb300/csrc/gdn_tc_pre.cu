@@ -190,10 +190,11 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
     const float G = __expf(gr), dte = __expf(sm.g[BT - 1] - gr);
     sm.G[tid] = G;
     sm.dte[tid] = dte;
-    float* dec = ws.dec + bh * 3 * BT;
+    float* dec = ws.dec + bh * TC_DEC_ROWS * BT;
     dec[tid] = G;
     dec[BT + tid] = dte;
     dec[2 * BT + tid] = gr;
+    dec[3 * BT + tid] = sm.b[tid];
   }
 
   // K K^T and Q K^T on rows [R0, R0 + 16), columns [32 cw, 32 cw + 32)
