@@ -97,8 +97,8 @@ struct TcWs {
   __nv_bfloat16* W;      // [nblk, H, BT, TC_LDK]          W = T diag(beta Gamma) K
   __nv_bfloat16* U;      // [nblk, H, dv/16, BT, TC_LDU]   U = T diag(beta) V, tile-major
   __nv_bfloat16* QKM;    // [nblk, H, BT, TC_LD64]         Q K^T * Mask (j <= r)
-  __nv_bfloat16* Kp;     // [nblk, H, BT, TC_LDK]          K rows (padded copy, zero past the end)
-  __nv_bfloat16* Qp;     // [nblk, H, BT, TC_LDK]          Q rows (padded copy, zero past the end)
+  __nv_bfloat16* Kp;     // [nblk, H, BT, TC_LDK]          K~ = e^{gamma_C - gamma} K (padded, zero past the end)
+  __nv_bfloat16* Qp;     // [nblk, H, BT, TC_LDK]          Q~ = e^{gamma} Q (padded, zero past the end)
   __nv_bfloat16* T;      // [nblk, H, BT, BT]      (I + A)^-1          (backward)
   __nv_bfloat16* KKM;    // [nblk, H, BT, TC_LD64] K K^T * Mask, strictly lower (backward)
   __nv_bfloat16* HbT;    // [nblk, H, dv, 128]     H_b^T               (backward)

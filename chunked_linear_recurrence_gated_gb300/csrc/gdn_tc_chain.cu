@@ -11,12 +11,14 @@
 // Compute warp w owns key columns [32w, 32w + 32) of the state and tokens
 // [16w, 16w + 16) of each block.
 //
-// Forward chain, per block (H^T: value rows x key columns):
-//   X^T    = H^T W^T ;  V^new^T = U^T - X^T ;  Vs^T = V^new^T * e^{gamma_C - gamma}
-//   H^T   <- Gamma_C H^T + Vs^T K
-//   O^T    = (H^T Q^T) * Gamma + V^new^T QKM^T         (forward mode only)
+// Pre hands over the decay-scaled copies K~ = diag(e^{gamma_C - gamma}) K and
+// Q~ = diag(e^{gamma}) Q, so every decay factor of a step except Gamma_C sits
+// in an operand. Forward chain, per block (H^T: value rows x key columns):
+//   X^T    = H^T W^T ;  V^new^T = U^T - X^T
+//   H^T   <- Gamma_C H^T + V^new^T K~
+//   O^T    = H^T Q~^T + V^new^T QKM^T                   (forward mode only)
 // Reverse chain, per block from the last one (dH = dS_out at the start):
-//   dV^new = QKM^T dO + Kt dH ;  dH <- Gamma_C dH + (Gamma Q)^T dO - W^T dV^new
+//   dV^new = QKM^T dO + K~ dH ;  dH <- Gamma_C dH + Q~^T dO - W^T dV^new
 // The backward call runs the recompute chain (which rebuilds H_b and V^new
 // from S_in) and the reverse chain concurrently: they depend only on Pre.
 #include "gdn_internal.cuh"
@@ -56,7 +58,6 @@ struct FwdSmem {
   uint64_t empty[fwd_stages<MODE, RG>()];
   __nv_bfloat16 HT[16 * RG * LDK];
   __nv_bfloat16 VnT[16 * RG * LD64];
-  __nv_bfloat16 VsT[16 * RG * LD64];
   __nv_bfloat16 O[MODE == CHAIN_FWD ? BT * (16 * RG + 8) : 8];
   int abort;
 };
@@ -167,7 +168,8 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
               *reinterpret_cast<const uint4*>(&sm.HT[r * LDK + c]);
         }
       }
-      // X^T = H^T W^T (and H^T Q^T); W / Q fragments are shared by the row groups
+      // X^T = H^T W^T (W fragments shared by the row groups) and, forward, H^T Q~^T
+      // from the same H^T fragments
       float x[RG][2][2][4], o1[RG][2][2][4];
 #pragma unroll
       for (int g = 0; g < RG; ++g)
@@ -191,24 +193,18 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
             mma16816(x[g][kc & 1][0], aH[kc], bW[kc][0], bW[kc][1]);
             mma16816(x[g][kc & 1][1], aH[kc], bW[kc][2], bW[kc][3]);
           }
-        }
-        if (MODE == CHAIN_FWD) {
-#pragma unroll
-          for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_x2n(bW[kc], S.Q, LDK, 16 * w, 16 * kc);
-#pragma unroll
-          for (int g = 0; g < RG; ++g) {
-            uint32_t aH[DK / 16][4];
-#pragma unroll
-            for (int kc = 0; kc < DK / 16; ++kc) lda_rm(aH[kc], sm.HT, LDK, 16 * g, 16 * kc);
+          if (MODE == CHAIN_FWD) {
 #pragma unroll
             for (int kc = 0; kc < DK / 16; ++kc) {
-              mma16816(o1[g][kc & 1][0], aH[kc], bW[kc][0], bW[kc][1]);
-              mma16816(o1[g][kc & 1][1], aH[kc], bW[kc][2], bW[kc][3]);
+              uint32_t bQ[4];
+              ldb_nk_x2n(bQ, S.Q, LDK, 16 * w, 16 * kc);
+              mma16816(o1[g][kc & 1][0], aH[kc], bQ[0], bQ[1]);
+              mma16816(o1[g][kc & 1][1], aH[kc], bQ[2], bQ[3]);
             }
           }
         }
       }
-      // V^new^T = U^T - X^T ; scaled copy for the state update
+      // V^new^T = U^T - X^T
 #pragma unroll
       for (int g = 0; g < RG; ++g)
 #pragma unroll
@@ -224,8 +220,6 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
             const float v1 = u1 - (x[g][0][j][2 * hf + 1] + x[g][1][j][2 * hf + 1]);
             const uint32_t pv = pack_bf16(v0, v1);
             *reinterpret_cast<uint32_t*>(&sm.VnT[vr * LD64 + t0]) = pv;
-            *reinterpret_cast<uint32_t*>(&sm.VsT[vr * LD64 + t0]) =
-                pack_bf16(v0 * dec[BT + t0], v1 * dec[BT + t0 + 1]);
             if (keep && ok)
               *reinterpret_cast<uint32_t*>(ws.VnT + bh * DV * BT + (size_t)(tile * BV + vr) * BT + t0) = pv;
           }
@@ -239,16 +233,12 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
       }
       named_bar(1, 128);
 
-      // H^T <- Gamma_C H^T + Vs^T K on key columns [32w, 32w + 32)
+      // H^T <- Gamma_C H^T + V^new^T K~ on key columns [32w, 32w + 32); forward:
+      // O^T = H_b^T Q~^T + V^new^T QKM^T from the same V^new^T fragments
       const float GC = dec[BT - 1];
-      float o2[RG][2][4];
 #pragma unroll
       for (int g = 0; g < RG; ++g) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o2[g][j][e] = 0.f;
-        float h2[4][4];
+        float h2[4][4], o2[2][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -258,7 +248,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
           }
         uint32_t aV[4][4];
 #pragma unroll
-        for (int kc = 0; kc < 4; ++kc) lda_rm(aV[kc], sm.VsT, LD64, 16 * g, 16 * kc);
+        for (int kc = 0; kc < 4; ++kc) lda_rm(aV[kc], sm.VnT, LD64, 16 * g, 16 * kc);
 #pragma unroll
         for (int kc = 0; kc < 4; ++kc) {
           float(*acc)[4] = (kc & 1) ? h2 : hs[g];
@@ -271,12 +261,20 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
           for (int e = 0; e < 4; ++e) hs[g][j][e] += h2[j][e];
         if (MODE == CHAIN_FWD) {
 #pragma unroll
-          for (int kc = 0; kc < 4; ++kc) lda_rm(aV[kc], sm.VnT, LD64, 16 * g, 16 * kc);
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o2[j][e] = o1[g][0][j][e] + o1[g][1][j][e];
 #pragma unroll
           for (int kc = 0; kc < 4; ++kc) {
-            mma16816(o2[g][0], aV[kc], bM[kc][0], bM[kc][1]);
-            mma16816(o2[g][1], aV[kc], bM[kc][2], bM[kc][3]);
+            mma16816(o2[0], aV[kc], bM[kc][0], bM[kc][1]);
+            mma16816(o2[1], aV[kc], bM[kc][2], bM[kc][3]);
           }
+          // O[token][v]: the transposing matrix store turns the (value, token)
+          // fragments into token rows for coalesced global stores
+          const int mi = l >> 3;
+          stsm_x4_t(smem_u32(&sm.O[(16 * w + 8 * (mi >> 1) + (l & 7)) * LDO + 16 * g + 8 * (mi & 1)]),
+                    pack_bf16(o2[0][0], o2[0][1]), pack_bf16(o2[0][2], o2[0][3]),
+                    pack_bf16(o2[1][0], o2[1][1]), pack_bf16(o2[1][2], o2[1][3]));
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -288,18 +286,6 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
           }
       }
       if (MODE == CHAIN_FWD) {
-        // O[token][v] = Gamma_token (H^T Q^T)^T + (V^new^T QKM^T)^T, staged for coalesced stores
-#pragma unroll
-        for (int g = 0; g < RG; ++g)
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int vr = 16 * g + gq + 8 * (e >> 1);
-              const int t = 16 * w + 8 * j + 2 * tq + (e & 1);
-              sm.O[t * LDO + vr] = __float2bfloat16_rn(
-                  dec[t] * (o1[g][0][j][e] + o1[g][1][j][e]) + o2[g][j][e]);
-            }
         __syncwarp();
         // each warp stores its own 16 tokens: BV / 8 chunks of 16 bytes per row
         for (int idx = l; idx < 16 * (BV / 8); idx += 32) {
@@ -350,7 +336,6 @@ struct RevSmem {
   uint64_t empty[REV_STAGES];
   __nv_bfloat16 dHT[16 * RG * LDK];   // bf16 copy of dH^T (value rows)
   __nv_bfloat16 dVT[16 * RG * LD64];  // -dV^new^T (value rows)
-  __nv_bfloat16 dOs[BT * (16 * RG + 8)];  // diag(Gamma) dO tile
   int abort;
 };
 
@@ -465,22 +450,7 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
               *reinterpret_cast<const uint4*>(&sm.dHT[r * LDK + c]);
         }
       }
-      // diag(Gamma) dO for the off-chain term (warp w: rows 16w..16w+15)
-      for (int idx = l; idx < 16 * (BV / 8); idx += 32) {
-        const int r = 16 * w + idx / (BV / 8), c = (idx % (BV / 8)) * 8;
-        const float G = dec[r];
-        const uint4 raw = *reinterpret_cast<const uint4*>(&S.dO[r * LDO + c]);
-        const uint32_t* pr = reinterpret_cast<const uint32_t*>(&raw);
-        uint4 outv;
-        uint32_t* po = reinterpret_cast<uint32_t*>(&outv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = unpack_bf16(pr[e]);
-          po[e] = pack_bf16(G * f.x, G * f.y);
-        }
-        *reinterpret_cast<uint4*>(&sm.dOs[r * LDO + c]) = outv;
-      }
-      // dV^new^T for tokens [16w, 16w + 16): dO^T QKM + (dH^T K^T) * e^{gamma_C - gamma}
+      // dV^new^T for tokens [16w, 16w + 16): dO^T QKM + dH^T K~^T
       {
         uint32_t bK[DK / 16][4], bM[4][4];
 #pragma unroll
@@ -515,9 +485,8 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
             for (int hf = 0; hf < 2; ++hf) {
               const int vr = 16 * g + gq + 8 * hf;
               const int t0 = 16 * w + 8 * j + 2 * tq;
-              const float d0 = a1[j][2 * hf] + dec[BT + t0] * (a2[0][j][2 * hf] + a2[1][j][2 * hf]);
-              const float d1 =
-                  a1[j][2 * hf + 1] + dec[BT + t0 + 1] * (a2[0][j][2 * hf + 1] + a2[1][j][2 * hf + 1]);
+              const float d0 = a1[j][2 * hf] + (a2[0][j][2 * hf] + a2[1][j][2 * hf]);
+              const float d1 = a1[j][2 * hf + 1] + (a2[0][j][2 * hf + 1] + a2[1][j][2 * hf + 1]);
               *reinterpret_cast<uint32_t*>(&sm.dVT[vr * LD64 + t0]) = pack_bf16(-d0, -d1);
               if (ok)
                 *reinterpret_cast<uint32_t*>(ws.dVnT + bh * DV * BT + (size_t)(tile * BV + vr) * BT + t0) =
@@ -535,7 +504,7 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
         ldb_kn_x2n(&bW[kc][4], S.W, LDK, 16 * kc, 32 * w + 16);
       }
       named_bar(1, 128);
-      // dH^T <- Gamma_C dH^T + (Gamma dO)^T Q - dV^new^T W on key columns [32w, 32w + 32)
+      // dH^T <- Gamma_C dH^T + dO^T Q~ - dV^new^T W on key columns [32w, 32w + 32)
       const float GC = dec[BT - 1];
 #pragma unroll
       for (int g = 0; g < RG; ++g) {
@@ -550,7 +519,7 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
         uint32_t aO[4][4], aV[4][4];
 #pragma unroll
         for (int kc = 0; kc < 4; ++kc) {
-          lda_tr(aO[kc], sm.dOs, LDO, 16 * g, 16 * kc);
+          lda_tr(aO[kc], S.dO, LDO, 16 * g, 16 * kc);
           lda_rm(aV[kc], sm.dVT, LD64, 16 * g, 16 * kc);
         }
 #pragma unroll

@@ -174,17 +174,6 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
   block_cumsum64(sm.g);
   cp_wait<0>();
   __syncthreads();
-  // padded copies of K and Q for the chains (one bulk copy each per block)
-  {
-    const uint4* sK = reinterpret_cast<const uint4*>(sm.K);
-    const uint4* sQ = reinterpret_cast<const uint4*>(sm.Q);
-    uint4* gK = reinterpret_cast<uint4*>(ws.Kp + bh * BT * LDK);
-    uint4* gQ = reinterpret_cast<uint4*>(ws.Qp + bh * BT * LDK);
-    for (int idx = tid; idx < BT * LDK / 8; idx += NT) {
-      gK[idx] = sK[idx];
-      gQ[idx] = sQ[idx];
-    }
-  }
   if (tid < BT) {
     const float gr = sm.g[tid];
     const float G = __expf(gr), dte = __expf(sm.g[BT - 1] - gr);
@@ -195,6 +184,30 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
     dec[BT + tid] = dte;
     dec[2 * BT + tid] = gr;
     dec[3 * BT + tid] = sm.b[tid];
+  }
+  __syncthreads();
+  // padded, decay-scaled copies for the chains (one bulk copy each per block):
+  // K~ = diag(e^{gamma_C - gamma}) K and Q~ = diag(e^{gamma}) Q
+  {
+    const uint4* sK = reinterpret_cast<const uint4*>(sm.K);
+    const uint4* sQ = reinterpret_cast<const uint4*>(sm.Q);
+    uint4* gK = reinterpret_cast<uint4*>(ws.Kp + bh * BT * LDK);
+    uint4* gQ = reinterpret_cast<uint4*>(ws.Qp + bh * BT * LDK);
+    for (int idx = tid; idx < BT * LDK / 8; idx += NT) {
+      const int r = idx / (LDK / 8);
+      const float sk = sm.dte[r], sq = sm.G[r];
+      uint4 a = sK[idx], b = sQ[idx];
+      uint32_t* pa = &a.x;
+      uint32_t* pb = &b.x;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = unpack_bf16(pa[e]), y = unpack_bf16(pb[e]);
+        pa[e] = pack_bf16(sk * x.x, sk * x.y);
+        pb[e] = pack_bf16(sq * y.x, sq * y.y);
+      }
+      gK[idx] = a;
+      gQ[idx] = b;
+    }
   }
 
   // K K^T and Q K^T on rows [R0, R0 + 16), columns [32 cw, 32 cw + 32)
