@@ -230,31 +230,38 @@ class Runner:
     def sl(self, t, i):
         return t[:, self.bounds[i]:self.bounds[i + 1]]
 
-    def step(self):
+    def fwd_chunk(self, i):
+        g, x = self.gdn, self.x
+        args = (self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
+                self.sl(x["g"], i), self.sl(x["beta"], i))
+        if self.reuse:
+            g.gdn_chunk_fwd_save(*args, S_in=self.S[i], saved=self.saved[i],
+                                 o=self.sl(self.o, i), S_out=self.S[i + 1], workspace=self.ws_s)
+        else:
+            g.gdn_chunk_fwd(*args, S_in=self.S[i], o=self.sl(self.o, i), S_out=self.S[i + 1],
+                            workspace=self.ws_f)
+
+    def bwd_chunk(self, i):
         g, x = self.gdn, self.x
         n = len(self.w.chunks)
+        args = (self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
+                self.sl(x["g"], i), self.sl(x["beta"], i), self.S[i], self.sl(x["do"], i))
+        grads = (self.sl(self.dq, i), self.sl(self.dk, i), self.sl(self.dv, i),
+                 self.sl(self.dg, i), self.sl(self.db, i))
+        dS_out = self.dS[i + 1] if i + 1 < n else None
+        if self.reuse:
+            g.gdn_chunk_bwd_saved(*args, self.saved[i], dS_out=dS_out, grads=grads,
+                                  dS_in=self.dS[i], workspace=self.ws_s)
+        else:
+            g.gdn_chunk_bwd(*args, dS_out=dS_out, grads=grads, dS_in=self.dS[i],
+                            workspace=self.ws_b)
+
+    def step(self):
+        n = len(self.w.chunks)
         for i in range(n):
-            args = (self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
-                    self.sl(x["g"], i), self.sl(x["beta"], i))
-            if self.reuse:
-                g.gdn_chunk_fwd_save(*args, S_in=self.S[i], saved=self.saved[i],
-                                     o=self.sl(self.o, i), S_out=self.S[i + 1],
-                                     workspace=self.ws_s)
-            else:
-                g.gdn_chunk_fwd(*args, S_in=self.S[i], o=self.sl(self.o, i),
-                                S_out=self.S[i + 1], workspace=self.ws_f)
+            self.fwd_chunk(i)
         for i in reversed(range(n)):
-            args = (self.sl(x["q"], i), self.sl(x["k"], i), self.sl(x["v"], i),
-                    self.sl(x["g"], i), self.sl(x["beta"], i), self.S[i], self.sl(x["do"], i))
-            grads = (self.sl(self.dq, i), self.sl(self.dk, i), self.sl(self.dv, i),
-                     self.sl(self.dg, i), self.sl(self.db, i))
-            dS_out = self.dS[i + 1] if i + 1 < n else None
-            if self.reuse:
-                g.gdn_chunk_bwd_saved(*args, self.saved[i], dS_out=dS_out, grads=grads,
-                                      dS_in=self.dS[i], workspace=self.ws_s)
-            else:
-                g.gdn_chunk_bwd(*args, dS_out=dS_out, grads=grads, dS_in=self.dS[i],
-                                workspace=self.ws_b)
+            self.bwd_chunk(i)
 
 
 def barrier(world):
@@ -287,24 +294,62 @@ def time_steps(fn, K, dev):
 
 
 def e2e_measure(runner, K, dev):
-    """Same step through the public API with host buffers: pinned host inputs
-    copied in and results (o and every gradient) copied out inside the timed region."""
+    """Same step through the public API with host buffers: every chunk's inputs
+    are copied in from pinned host memory and its results (o and every
+    gradient) copied out inside the timed region. The copies run per chunk on
+    two copy streams, overlapped with the kernels of the neighbouring chunks;
+    a step starts only after the previous one has finished."""
     x = runner.x
     keys = ["q", "k", "v", "g", "beta", "do"]
     host_in = {k: torch.empty(x[k].shape, dtype=x[k].dtype, pin_memory=True) for k in keys}
     for k in keys:
         host_in[k].copy_(x[k])
-    outs = [runner.o, runner.dq, runner.dk, runner.dv, runner.dg, runner.db]
+    outs = [runner.dq, runner.dk, runner.dv, runner.dg, runner.db]
+    host_o = torch.empty(runner.o.shape, dtype=runner.o.dtype, pin_memory=True)
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    d2h = host_o.numel() * host_o.element_size() + sum(t.numel() * t.element_size() for t in host_out)
+    comp = torch.cuda.current_stream(dev)
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    n = len(runner.w.chunks)
+
+    fwd_keys = ["q", "k", "v", "g", "beta"]
 
     def one():
-        for k in keys:
-            x[k].copy_(host_in[k], non_blocking=True)
-        runner.step()
-        for h, t in zip(host_out, outs):
-            h.copy_(t, non_blocking=True)
+        s_in.wait_stream(comp)
+        ready, ready_do = [], [None] * n
+        with torch.cuda.stream(s_in):
+            # forward inputs in chunk order, then dO in the backward's (reverse) order
+            for i in range(n):
+                for k in fwd_keys:
+                    runner.sl(x[k], i).copy_(runner.sl(host_in[k], i), non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_in)
+                ready.append(ev)
+            for i in reversed(range(n)):
+                runner.sl(x["do"], i).copy_(runner.sl(host_in["do"], i), non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_in)
+                ready_do[i] = ev
+        for i in range(n):
+            comp.wait_event(ready[i])
+            runner.fwd_chunk(i)
+            done = torch.cuda.Event()
+            done.record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                runner.sl(host_o, i).copy_(runner.sl(runner.o, i), non_blocking=True)
+        for i in reversed(range(n)):
+            comp.wait_event(ready_do[i])
+            runner.bwd_chunk(i)
+            done = torch.cuda.Event()
+            done.record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                for h, t in zip(host_out, outs):
+                    runner.sl(h, i).copy_(runner.sl(t, i), non_blocking=True)
+        comp.wait_stream(s_out)
 
     one()
     ms = time_steps(one, K, dev)
@@ -476,7 +521,9 @@ def main():
     if not args.no_e2e:
         e_ms, h2d, d2h = e2e_measure(runner, max(1, min(args.steps, 3)), dev)
         e2e = {"value": tokens / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "copies": "pinned host buffers, per chunk on two copy streams overlapped "
+                         "with the kernels"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, runner.x)
