@@ -16,6 +16,9 @@ Two independent formulations live here:
   V^new of Eq. 2, kernel-level blocks b_{i,j}) in numpy fp64, written from its
   derivation; the tests check it against the token loop, which pins the
   chunkwise algebra the GPU kernels implement.
+* ``short_conv``: the causal short convolution with its carried boundary
+  state (the auxiliary local-convolution states of the StateFlow review) and
+  its reverse-mode derivative, numpy fp64.
 
 Array layouts: q, k [B, T, H, dk]; v, o [B, T, H, dv]; g, beta [B, T, H];
 states [B, H, dk, dv] holding S^T (o_t = state^T q_t). Varlen: B = 1 and
