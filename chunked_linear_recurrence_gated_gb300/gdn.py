@@ -29,6 +29,9 @@ EXPORTS = ["gdn_chunk_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "gdn_chunk_fwd_noalloc", "gdn_chunk_saved_bytes", "gdn_chunk_fwd_save",
            "gdn_chunk_bwd_saved"]
 GDN_WS_SAVED = 2
+# include/gdn_conv.h
+CONV_EXPORTS = ["gdn_conv_workspace_bytes", "gdn_conv_fwd", "gdn_conv_bwd"]
+CONV_ACT = {"none": 0, "silu": 1}
 
 
 class GdnError(RuntimeError):
@@ -40,6 +43,11 @@ class GdnError(RuntimeError):
 class gdn_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class gdn_conv_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("C", ctypes.c_int),
+                ("W", ctypes.c_int), ("dtype", ctypes.c_int), ("act", ctypes.c_int)]
 
 
 _lib = None
@@ -89,6 +97,13 @@ def load(build_if_missing: bool = False):
     lib.gdn_chunk_fwd_save.restype = I
     lib.gdn_chunk_bwd_saved.argtypes = [SP] + [P] * 14 + [P, Z, P, Z, P]
     lib.gdn_chunk_bwd_saved.restype = I
+    CP = ctypes.POINTER(gdn_conv_shape)
+    lib.gdn_conv_workspace_bytes.argtypes = [CP]
+    lib.gdn_conv_workspace_bytes.restype = Z
+    lib.gdn_conv_fwd.argtypes = [CP] + [P] * 6 + [P]
+    lib.gdn_conv_fwd.restype = I
+    lib.gdn_conv_bwd.argtypes = [CP] + [P] * 10 + [P, Z, P]
+    lib.gdn_conv_bwd.restype = I
     lib.gdn_profile_arm.argtypes = [P, I]
     lib.gdn_profile_arm.restype = None
     lib.gdn_profile_count.argtypes = []
@@ -285,6 +300,50 @@ def gdn_varlen_bwd(cu_seqlens, q, k, v, g, beta, S0, dout, dS_final=None, grads=
                             _p(dS0), _p(workspace), workspace.numel(), _stream(stream))
     _check(rc, "gdn_varlen_bwd")
     return (*grads, dS0)
+
+
+def conv_shape_of(x: torch.Tensor, w: torch.Tensor, act: str) -> gdn_conv_shape:
+    B, T, C = x.shape
+    return gdn_conv_shape(B, T, C, w.shape[1], _dtype_code(x), CONV_ACT[act])
+
+
+def gdn_conv_fwd(x, w, b=None, state_in=None, act="silu", y=None, state_out=None,
+                 want_state=True, stream=None):
+    """Causal short convolution of one chunk, x [B, T, C]. Returns (y, state_out [B, W-1, C])."""
+    lib = load()
+    s = conv_shape_of(x, w, act)
+    B, T, C = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    if state_out is None and want_state:
+        state_out = torch.empty(B, w.shape[1] - 1, C, dtype=x.dtype, device=x.device)
+    rc = lib.gdn_conv_fwd(ctypes.byref(s), _p(x), _p(w), _p(b), _p(state_in), _p(y),
+                          _p(state_out), _stream(stream))
+    _check(rc, "gdn_conv_fwd")
+    return y, state_out
+
+
+def gdn_conv_bwd(x, w, b, state_in, dy, dstate_out=None, act="silu", dx=None, dw=None,
+                 db=None, dstate_in=None, workspace=None, stream=None, want_state=True):
+    """Backward of one chunk. Returns (dx, dw, db, dstate_in)."""
+    lib = load()
+    s = conv_shape_of(x, w, act)
+    B, T, C = x.shape
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty_like(w)
+    if db is None and b is not None:
+        db = torch.empty_like(b)
+    if dstate_in is None and want_state:
+        dstate_in = torch.empty(B, w.shape[1] - 1, C, dtype=x.dtype, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(lib.gdn_conv_workspace_bytes(ctypes.byref(s)), x.device)
+    rc = lib.gdn_conv_bwd(ctypes.byref(s), _p(x), _p(w), _p(b), _p(state_in), _p(dy),
+                          _p(dstate_out), _p(dx), _p(dw), _p(db), _p(dstate_in), _p(workspace),
+                          workspace.numel(), _stream(stream))
+    _check(rc, "gdn_conv_bwd")
+    return dx, dw, db, dstate_in
 
 
 def gdn_workspace_status(workspace, stream=None) -> int:

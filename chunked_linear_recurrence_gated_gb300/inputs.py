@@ -135,3 +135,28 @@ def make_inputs(B, T, H, dk, dv, dtype=torch.bfloat16, seed=1234, device="cpu",
 def make_workload_inputs(w: Workload, device="cpu", **kw):
     return make_inputs(w.B, w.T, w.H, w.dk, w.dv, dtype=w.torch_dtype, seed=w.seed,
                        device=device, do_scale=w.do_scale, **kw)
+
+
+# ---------------------------------------------------------------- short convolution
+# Recipe for the causal short convolution carried across chunks (the auxiliary
+# local-convolution states): x ~ N(0, 1), weights ~ N(0, 1) / sqrt(W),
+# bias ~ 0.1 N(0, 1), incoming state ~ N(0, 1) (zeros at a sequence start),
+# dy ~ N(0, 1), dstate_out ~ N(0, 1). The benchmark's case is a Gated DeltaNet
+# layer's q / k / v convolution on the 256K-token workload: C = 16 heads x
+# (128 + 128 + 128) channels, W = 4, SiLU, 8 chained chunks of 32768 tokens.
+CONV_BENCH = dict(B=1, T=262144, C=16 * 384, W=4, chunks=[32768] * 8, act="silu")
+
+
+def make_conv_inputs(B, T, C, W, dtype=torch.bfloat16, seed=4321, device="cpu",
+                     with_state=True, with_bias=True):
+    gen = torch.Generator().manual_seed(seed)
+    r = lambda *shape: torch.randn(*shape, generator=gen, dtype=torch.float32)
+    out = {
+        "x": r(B, T, C).to(dtype),
+        "w": r(C, W) / math.sqrt(W),
+        "b": 0.1 * r(C) if with_bias else None,
+        "dy": r(B, T, C).to(dtype),
+        "state_in": r(B, W - 1, C).to(dtype) if with_state else None,
+        "dstate_out": r(B, W - 1, C).to(dtype) if with_state else None,
+    }
+    return {k: (v.to(device) if v is not None else None) for k, v in out.items()}

@@ -18,18 +18,19 @@ def lib():
     return gdn.load()
 
 
-def header_functions():
-    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+def header_functions(name="gdn.h"):
+    text = open(os.path.join(ROOT, "include", name)).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
 
 
 def test_header_and_binding_agree():
     assert header_functions() == sorted(gdn.EXPORTS)
+    assert header_functions("gdn_conv.h") == sorted(gdn.CONV_EXPORTS)
 
 
 def test_library_exports_every_header_symbol(lib):
-    for name in header_functions():
+    for name in header_functions() + header_functions("gdn_conv.h"):
         assert hasattr(lib, name), name
 
 
@@ -141,3 +142,33 @@ def test_saved_products_sizes_and_checks(lib):
     assert rc == 3                                      # workspace too small
     rc = lib.gdn_chunk_bwd_saved(ctypes.byref(s), *bwd_args, None, saved, P(FAKE), ws_saved, None)
     assert rc == 3
+
+
+def conv_shape(B=2, T=100, C=64, W=4, dtype=1, act=1):
+    return gdn.gdn_conv_shape(B, T, C, W, dtype, act)
+
+
+def test_conv_host_checks(lib):
+    P = ctypes.c_void_p
+    ws = lib.gdn_conv_workspace_bytes(ctypes.byref(conv_shape()))
+    assert ws > 0 and ws % 256 == 0
+    assert lib.gdn_conv_workspace_bytes(ctypes.byref(conv_shape(W=9))) == 0
+    assert lib.gdn_conv_workspace_bytes(ctypes.byref(conv_shape(C=66))) == 0
+
+    def fwd(s, x=FAKE, w=FAKE, b=None, si=None, y=FAKE, so=FAKE):
+        return lib.gdn_conv_fwd(ctypes.byref(s), *[P(v) if v else None for v in (x, w, b, si, y, so)],
+                                None)
+
+    assert fwd(conv_shape(B=0)) == 1
+    assert fwd(conv_shape(act=3)) == 1
+    assert fwd(conv_shape(W=1)) == 2
+    assert fwd(conv_shape(C=6)) == 2
+    assert fwd(conv_shape(dtype=5)) == 2
+    assert fwd(conv_shape(), x=FAKE + 8) == 1          # misaligned input
+    assert fwd(conv_shape(), w=None) == 1              # weights required
+    assert fwd(conv_shape(), si=FAKE, so=FAKE) == 1    # state_out aliases state_in
+    s = conv_shape()
+    args = [P(FAKE)] * 2 + [None, None, P(FAKE), None, P(FAKE), P(FAKE), None, None]
+    assert lib.gdn_conv_bwd(ctypes.byref(s), *args, None, ws, None) == 3
+    assert lib.gdn_conv_bwd(ctypes.byref(s), *args, P(FAKE), ws - 256, None) == 3
+    assert lib.gdn_conv_bwd(ctypes.byref(s), *args, P(FAKE + 16), ws, None) == 3
