@@ -15,6 +15,7 @@ scaling; heads and sequences share nothing, so there is no collective) and
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import subprocess
@@ -356,6 +357,62 @@ def e2e_measure(runner, K, dev):
     return ms / K, h2d, d2h
 
 
+def conv_measure(K, warmup, dev, hbm, peak_kind):
+    """The causal short convolution carried across chunks (the auxiliary
+    local-convolution states), measured on a Gated DeltaNet layer's q / k / v
+    convolution of the same 256K-token sequence: fwd over the 8 chained chunks,
+    then bwd in reverse order. Algorithmic bytes: fwd reads x and writes y, bwd
+    reads x and dy and writes dx (bf16), plus the (W - 1)-row states."""
+    from chunked_linear_recurrence_gated_gb300 import gdn
+    from chunked_linear_recurrence_gated_gb300.inputs import CONV_BENCH, make_conv_inputs
+
+    cfg = CONV_BENCH
+    B, T, C, W, act = cfg["B"], cfg["T"], cfg["C"], cfg["W"], cfg["act"]
+    d = make_conv_inputs(B, T, C, W, dtype=torch.bfloat16, device=dev, with_state=False)
+    y = torch.empty_like(d["x"])
+    dx = torch.empty_like(d["x"])
+    n = len(cfg["chunks"])
+    bounds = np.concatenate([[0], np.cumsum(cfg["chunks"])]).astype(int)
+    st = [None] + [torch.empty(B, W - 1, C, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    dst = [torch.empty(B, W - 1, C, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    dws = [torch.empty_like(d["w"]) for _ in range(n)]
+    dbs = [torch.empty_like(d["b"]) for _ in range(n)]
+    shp = gdn.gdn_conv_shape(B, max(cfg["chunks"]), C, W, 1, gdn.CONV_ACT[act])
+    ws = gdn.alloc_workspace(gdn.load().gdn_conv_workspace_bytes(ctypes.byref(shp)), dev)
+    sl = lambda t, i: t[:, bounds[i]:bounds[i + 1]]
+
+    def step():
+        for i in range(n):
+            gdn.gdn_conv_fwd(sl(d["x"], i), d["w"], d["b"], st[i], act, y=sl(y, i),
+                             state_out=st[i + 1])
+        for i in reversed(range(n)):
+            gdn.gdn_conv_bwd(sl(d["x"], i), d["w"], d["b"], st[i], sl(d["dy"], i),
+                             dst[i + 1] if i + 1 < n else None, act, dx=sl(dx, i), dw=dws[i],
+                             db=dbs[i], dstate_in=dst[i], workspace=ws)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    ms = time_steps(step, K, dev) / K
+    timer = gdn.KernelTimer(capacity=512)
+    with timer:
+        step()
+    torch.cuda.synchronize(dev)
+    per = {k: sum(v) for k, v in timer.per_kernel().items()}
+    elems = B * T * C
+    alg = 5 * 2 * elems  # bytes
+    kb = {"conv_fwd": 2 * 2 * elems, "conv_bwd": 3 * 2 * elems}
+    kernels = {k: {"ms_per_step": v, "alg_gb_per_s": (kb[k] / (v / 1e3) / 1e9) if k in kb else None,
+                   "frac": (kb[k] / (v / 1e3) / 1e9 / hbm) if k in kb else None}
+               for k, v in per.items()}
+    return {"workload": f"qkv short conv B{B} T{T} C{C} W{W} {act} bf16, 8 x 32768 chained",
+            "ms_per_step": ms, "tokens_per_s": B * T / (ms / 1e3),
+            "alg_bytes_per_step": alg,
+            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": alg / (ms / 1e3) / 1e9 / hbm,
+                         "peak_source": peak_kind},
+            "kernels": kernels}
+
+
 def cpu_baseline(w, x, max_tokens=32768):
     """The oracle, as it stands, on a bounded sample: all heads of the first chunk."""
     import oracle
@@ -417,6 +474,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
                     help="workload index (1-3: fixed-length chunked bf16 workloads)")
+    ap.add_argument("--no-conv", action="store_true",
+                    help="skip the short-convolution measurement")
     ap.add_argument("--recompute", action="store_true",
                     help="backward recomputes the per-block Pre products instead of reading "
                          "the ones its chunk's forward kept")
@@ -524,6 +583,9 @@ def main():
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "copies": "pinned host buffers, per chunk on two copy streams overlapped "
                          "with the kernels"}
+    conv = None
+    if not args.no_conv and not args.tokens:
+        conv = conv_measure(max(3, min(args.steps, 10)), args.warmup, dev, hbm, peak_kind)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, runner.x)
@@ -547,6 +609,7 @@ def main():
             "op_roofline": op_roofline,
             "kernels_ms_per_step": {k: v / nsteps_timed for k, v in totals.items()},
             "cpu_baseline": cpu,
+            "short_conv": conv,
         }
         print(json.dumps(line))
     if world > 1:

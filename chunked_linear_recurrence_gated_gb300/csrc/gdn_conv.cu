@@ -12,6 +12,8 @@
 // 512-byte (fp32) segment.
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "../../include/gdn_conv.h"
 #include "gdn_internal.cuh"
 
@@ -55,12 +57,12 @@ __device__ __forceinline__ void zero_vec(float* v) {
 }
 
 __device__ __forceinline__ float act_fwd(float z, int act) {
-  return act ? z / (1.f + __expf(-z)) : z;
+  return act ? __fdividef(z, 1.f + __expf(-z)) : z;
 }
 // d act / dz
 __device__ __forceinline__ float act_grad(float z, int act) {
   if (!act) return 1.f;
-  const float s = 1.f / (1.f + __expf(-z));
+  const float s = __fdividef(1.f, 1.f + __expf(-z));
   return s * (1.f + z * (1.f - s));
 }
 
@@ -181,78 +183,98 @@ __global__ void __launch_bounds__(CONV_NT) k_conv_bwd(int Tn, int C, int act, co
   for (int v = 0; v < CV; ++v)
 #pragma unroll
     for (int j = 0; j < W; ++j) pw[v][j] = 0.f;
-  for (int t0 = tb; t0 < te; t0 += LA) {
+  // One token t: g[t] (zero outside [0, T)), this tile's partial sums, and
+  // dx_ext at x index t - (W - 1). GENERAL handles the tile's edges; the
+  // interior (g computed, owned, emitted into dx, no dstate_out) skips the tests.
+  auto step = [&](int t, const float* xc, const float* dd, auto general) {
+    constexpr bool GEN = decltype(general)::value;
+    float g[CV];
+    if (!GEN || (t >= 0 && t < Tn)) {
+      const bool own = !GEN || (t >= s0 && t < s1);
+#pragma unroll
+      for (int v = 0; v < CV; ++v) {
+        float z = br[v];
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) z = fmaf(wr[v][j], xw[j][v], z);
+        z = fmaf(wr[v][W - 1], xc[v], z);
+        g[v] = dd[v] * act_grad(z, act);
+        if (own) {
+          pb[v] += g[v];
+#pragma unroll
+          for (int j = 0; j < W - 1; ++j) pw[v][j] = fmaf(g[v], xw[j][v], pw[v][j]);
+          pw[v][W - 1] = fmaf(g[v], xc[v], pw[v][W - 1]);
+        }
+      }
+    } else {
+      zero_vec(g);
+    }
+    const int s = t - (W - 1);
+    if (!GEN || (s >= e0 && s < s1)) {
+      float o[CV];
+#pragma unroll
+      for (int v = 0; v < CV; ++v) {
+        float a = wr[v][0] * g[v];
+#pragma unroll
+        for (int j = 1; j < W; ++j) a = fmaf(wr[v][j], gw[W - 1 - j][v], a);
+        o[v] = a;
+      }
+      const int p = s + W - 1;  // index in x_ext
+      if (GEN && dsr && p >= Tn) {
+        float e[CV];
+        ld_vec(dsr + (size_t)(p - Tn) * C, e);
+#pragma unroll
+        for (int v = 0; v < CV; ++v) o[v] += e[v];
+      }
+      if (!GEN || s >= 0)
+        st_vec(dxr + (size_t)s * C, o);
+      else if (dsi)
+        st_vec(dsi + (size_t)p * C, o);
+    }
+#pragma unroll
+    for (int j = 0; j < W - 2; ++j)
+#pragma unroll
+      for (int v = 0; v < CV; ++v) {
+        xw[j][v] = xw[j + 1][v];
+        gw[j][v] = gw[j + 1][v];
+      }
+#pragma unroll
+    for (int v = 0; v < CV; ++v) {
+      xw[W - 2][v] = xc[v];
+      gw[W - 2][v] = g[v];
+    }
+  };
+  auto general_range = [&](int ta, int tz) {
+    for (int t = ta; t < tz; ++t) {
+      float xc[CV], dd[CV];
+      ld_ext<T, W>(xr, sr, t, Tn, C, xc);
+      if (t >= 0 && t < Tn)
+        ld_vec(gr + (size_t)t * C, dd);
+      else
+        zero_vec(dd);
+      step(t, xc, dd, std::true_type());
+    }
+  };
+  // interior: 0 <= t - (W - 1), s0 <= t - (W - 1), t < s1 (<= T)
+  const int m0 = max(tb + (W - 1), W - 1), m1 = max(m0, s1);
+  general_range(tb, min(m0, te));
+  int t = m0;
+  for (; t + LA <= m1; t += LA) {
     float xc[LA][CV], dd[LA][CV];
 #pragma unroll
     for (int u = 0; u < LA; ++u) {
-      const int t = t0 + u;
-      ld_ext<T, W>(xr, sr, t < te ? t : Tn, Tn, C, xc[u]);
-      if (t >= 0 && t < Tn && t < te)
-        ld_vec(gr + (size_t)t * C, dd[u]);
-      else
-        zero_vec(dd[u]);
+      ld_vec(xr + (size_t)(t + u) * C, xc[u]);
+      ld_vec(gr + (size_t)(t + u) * C, dd[u]);
     }
 #pragma unroll
-    for (int u = 0; u < LA; ++u) {
-      const int t = t0 + u;
-      if (t >= te) break;
-      float g[CV];
-      if (t >= 0 && t < Tn) {
-        const bool own = t >= s0 && t < s1;
-#pragma unroll
-        for (int v = 0; v < CV; ++v) {
-          float z = br[v];
-#pragma unroll
-          for (int j = 0; j < W - 1; ++j) z = fmaf(wr[v][j], xw[j][v], z);
-          z = fmaf(wr[v][W - 1], xc[u][v], z);
-          g[v] = dd[u][v] * act_grad(z, act);
-          if (own) {
-            pb[v] += g[v];
-#pragma unroll
-            for (int j = 0; j < W - 1; ++j) pw[v][j] = fmaf(g[v], xw[j][v], pw[v][j]);
-            pw[v][W - 1] = fmaf(g[v], xc[u][v], pw[v][W - 1]);
-          }
-        }
-      } else {
-        zero_vec(g);
-      }
-      // dx_ext at x index s = t - (W - 1): sum_j w[j] g[t - j]
-      const int s = t - (W - 1);
-      if (s >= e0 && s < s1) {
-        float o[CV];
-#pragma unroll
-        for (int v = 0; v < CV; ++v) {
-          float a = wr[v][0] * g[v];
-#pragma unroll
-          for (int j = 1; j < W; ++j) a = fmaf(wr[v][j], gw[W - 1 - j][v], a);
-          o[v] = a;
-        }
-        const int p = s + W - 1;  // index in x_ext
-        if (dsr && p >= Tn) {
-          float e[CV];
-          ld_vec(dsr + (size_t)(p - Tn) * C, e);
-#pragma unroll
-          for (int v = 0; v < CV; ++v) o[v] += e[v];
-        }
-        if (s >= 0)
-          st_vec(dxr + (size_t)s * C, o);
-        else if (dsi)
-          st_vec(dsi + (size_t)p * C, o);
-      }
-#pragma unroll
-      for (int j = 0; j < W - 2; ++j)
-#pragma unroll
-        for (int v = 0; v < CV; ++v) {
-          xw[j][v] = xw[j + 1][v];
-          gw[j][v] = gw[j + 1][v];
-        }
-#pragma unroll
-      for (int v = 0; v < CV; ++v) {
-        xw[W - 2][v] = xc[u][v];
-        gw[W - 2][v] = g[v];
-      }
-    }
+    for (int u = 0; u < LA; ++u) step(t + u, xc[u], dd[u], std::false_type());
   }
+  for (; t < m1; ++t) {
+    float xc[CV], dd[CV];
+    ld_vec(xr + (size_t)t * C, xc);
+    ld_vec(gr + (size_t)t * C, dd);
+    step(t, xc, dd, std::false_type());
+  }
+  general_range(max(m1, min(m0, te)), te);
   float* pp = part + (((size_t)bb * ntiles + tile) * C + c0) * (W + 1);
 #pragma unroll
   for (int v = 0; v < CV; ++v) {
