@@ -6,7 +6,7 @@
 //
 // HBM-bound: every thread owns 4 channels over a run of tokens, keeps the last
 // W - 1 inputs in registers as a sliding window, and reads each input row once
-// (plus a W - 1 row halo per tile), loading LA tokens ahead of their use so
+// (plus a W - 1 row halo per tile), loading LA_F / LA_B tokens ahead of their use so
 // that enough bytes are in flight. Consecutive threads take consecutive
 // channel groups, so every warp load is one contiguous 256-byte (bf16) or
 // 512-byte (fp32) segment.
@@ -25,7 +25,8 @@ constexpr int CONV_TTB = 256;  // tokens per backward tile (one dw / db partial 
 constexpr int CONV_NT = 128;   // threads per block
 
 constexpr int CV = 4;          // channels per thread
-constexpr int LA = 4;          // tokens loaded ahead of their use
+constexpr int LA_F = 4;        // tokens loaded ahead of their use (forward)
+constexpr int LA_B = 8;        // and in the backward's interior
 
 // 4 channels: 16 bytes of fp32 or 8 bytes of bf16
 __device__ __forceinline__ void ld_vec(const float* p, float* v) {
@@ -102,12 +103,12 @@ __global__ void __launch_bounds__(CONV_NT) k_conv_fwd(int Tn, int C, int act, co
 #pragma unroll
   for (int j = 0; j < W - 1; ++j) ld_ext<T, W>(xr, sr, t0 - (W - 1) + j, Tn, C, xw[j]);
   T* yr = y + (size_t)bb * Tn * C + c0;
-  for (int t = t0; t < t1; t += LA) {
-    float xc[LA][CV];
+  for (int t = t0; t < t1; t += LA_F) {
+    float xc[LA_F][CV];
 #pragma unroll
-    for (int u = 0; u < LA; ++u) ld_ext<T, W>(xr, sr, t + u < t1 ? t + u : Tn, Tn, C, xc[u]);
+    for (int u = 0; u < LA_F; ++u) ld_ext<T, W>(xr, sr, t + u < t1 ? t + u : Tn, Tn, C, xc[u]);
 #pragma unroll
-    for (int u = 0; u < LA; ++u) {
+    for (int u = 0; u < LA_F; ++u) {
       if (t + u < t1) {
         float out[CV];
 #pragma unroll
@@ -258,15 +259,15 @@ __global__ void __launch_bounds__(CONV_NT) k_conv_bwd(int Tn, int C, int act, co
   const int m0 = max(tb + (W - 1), W - 1), m1 = max(m0, s1);
   general_range(tb, min(m0, te));
   int t = m0;
-  for (; t + LA <= m1; t += LA) {
-    float xc[LA][CV], dd[LA][CV];
+  for (; t + LA_B <= m1; t += LA_B) {
+    float xc[LA_B][CV], dd[LA_B][CV];
 #pragma unroll
-    for (int u = 0; u < LA; ++u) {
+    for (int u = 0; u < LA_B; ++u) {
       ld_vec(xr + (size_t)(t + u) * C, xc[u]);
       ld_vec(gr + (size_t)(t + u) * C, dd[u]);
     }
 #pragma unroll
-    for (int u = 0; u < LA; ++u) step(t + u, xc[u], dd[u], std::false_type());
+    for (int u = 0; u < LA_B; ++u) step(t + u, xc[u], dd[u], std::false_type());
   }
   for (; t < m1; ++t) {
     float xc[CV], dd[CV];
