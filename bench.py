@@ -430,6 +430,15 @@ def cpu_baseline(w, x, max_tokens=32768):
                       f"(fp64 token loop, {dt:.1f} s)"}
 
 
+def workload_config(w, world, recompute):
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+            "chunks": w.chunks, "state": "fp32",
+            "backward": ("recomputes the Pre products" if recompute else
+                         "reads the Pre products its chunk's forward kept"),
+            "l2": "inputs larger than L2 (no flush)",
+            "parallelism": f"dp{world} (independent sequence per GPU)"}
+
+
 def reference_arm(args, w):
     """The oracle timed on the host cores, a bounded sample per step."""
     import oracle
@@ -454,10 +463,12 @@ def reference_arm(args, w):
     value = L / dt
     sample = f"fwd+bwd of the first {L} tokens, all {w.H} heads, per step"
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "sample_tokens": L},
+        "data": "synthetic",
+        "config": dict(workload_config(w, args.gpus, args.recompute), sample_tokens=L,
+                       runs_on=f"host cores of rank 0 ({threads} threads)"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(threads, w.H),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -596,12 +607,7 @@ def main():
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk,
-                       "dv": w.dv, "chunks": w.chunks, "state": "fp32",
-                       "backward": ("recomputes the Pre products" if args.recompute else
-                                    "reads the Pre products its chunk's forward kept"),
-                       "l2": "inputs larger than L2 (no flush)",
-                       "parallelism": f"dp{world} (independent sequence per GPU)"},
+            "config": workload_config(w, world, args.recompute),
             "clocks": clk.summary(),
             "e2e": e2e,
             "gpu_launches": launches * args.steps,
