@@ -327,6 +327,20 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
         }
     }
   }
+  // zero the pad columns of the padded tiles: every 32-byte sector is then
+  // written in full, so none has to be read back from DRAM to merge it
+  {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    __nv_bfloat16* W = ws.W + bh * BT * LDK;
+    __nv_bfloat16* qkm = ws.QKM + bh * BT * LD64;
+    __nv_bfloat16* U = ws.U + bh * (DV / 16) * BT * LDU;
+    for (int r = tid; r < BT; r += NT) {
+      *reinterpret_cast<uint4*>(W + r * LDK + DK) = z;
+      *reinterpret_cast<uint4*>(qkm + r * LD64 + BT) = z;
+      if (ws.KKM) *reinterpret_cast<uint4*>(ws.KKM + bh * BT * LD64 + r * LD64 + BT) = z;
+    }
+    for (int r = tid; r < (DV / 16) * BT; r += NT) *reinterpret_cast<uint4*>(U + r * LDU + 16) = z;
+  }
 }
 
 template <class K>
