@@ -108,3 +108,66 @@ def test_fp32_workload_sizes_on_simt_path():
     import ctypes
     assert lib.gdn_path(ctypes.byref(s0)) == 1
     assert lib.gdn_path(ctypes.byref(s2)) == 2
+
+
+def test_benchmark_step_kept_products():
+    """The benchmark's own step (bench.Runner: 8 chained 32768-token chunks,
+    forward keeping its products, backward reading them) on the 256K-token
+    workload: sampled heads against the oracle, and every output bitwise equal
+    to the recomputing pair."""
+    import bench
+
+    w = workload(2)
+    dev = torch.device("cuda", 0)
+    kept = bench.Runner(w, dev, reuse=True)
+    kept.step()
+    torch.cuda.synchronize()
+    grads = (kept.dq, kept.dk, kept.dv, kept.dg, kept.db, kept.dS[0])
+    check_heads(w, kept.x, kept.o, kept.S[-1], grads, [0, 9])
+    outs = [t.clone() for t in (kept.o, kept.S[-1]) + grads]
+    del kept
+    torch.cuda.empty_cache()
+    rec = bench.Runner(w, dev, reuse=False)
+    rec.step()
+    torch.cuda.synchronize()
+    for a, b in zip(outs, (rec.o, rec.S[-1], rec.dq, rec.dk, rec.dv, rec.dg, rec.db, rec.dS[0])):
+        assert torch.equal(a, b)
+
+
+def test_benchmark_short_conv_full_size():
+    """The benchmark's short convolution (C = 6144, W = 4, SiLU, 256K tokens in
+    8 chained chunks) on sampled channels against the oracle; the chained
+    forward equals one call over the whole sequence."""
+    from chunked_linear_recurrence_gated_gb300.inputs import CONV_BENCH, make_conv_inputs
+    from oracle import short_conv as sc
+
+    cfg = CONV_BENCH
+    B, T, C, W = cfg["B"], cfg["T"], cfg["C"], cfg["W"]
+    d = make_conv_inputs(B, T, C, W, dtype=BF, device="cuda", with_state=False)
+    bounds = np.concatenate([[0], np.cumsum(cfg["chunks"])]).astype(int)
+    n = len(cfg["chunks"])
+    ys, states, s = [], [None], None
+    for i in range(n):
+        y, s = gdn.gdn_conv_fwd(d["x"][:, bounds[i]:bounds[i + 1]], d["w"], d["b"], s, "silu")
+        ys.append(y)
+        states.append(s)
+    dxs, dw, db, ds = [None] * n, 0, 0, None
+    for i in reversed(range(n)):
+        sl = slice(bounds[i], bounds[i + 1])
+        dx, dwi, dbi, ds = gdn.gdn_conv_bwd(d["x"][:, sl], d["w"], d["b"], states[i],
+                                            d["dy"][:, sl], ds, "silu")
+        dxs[i] = dx
+        dw, db = dw + dwi, db + dbi
+    y_full, _ = gdn.gdn_conv_fwd(d["x"], d["w"], d["b"], None, "silu")
+    torch.cuda.synchronize()
+    y = torch.cat(ys, dim=1)
+    assert torch.equal(y, y_full)
+    cols = torch.arange(3, C, 389)
+    f64 = lambda t: t.double().cpu().numpy()
+    y_ref, _ = sc.conv_fwd(f64(d["x"][..., cols]), f64(d["w"][cols]), f64(d["b"][cols]), None)
+    dx_ref, dw_ref, db_ref, _ = sc.conv_bwd(f64(d["x"][..., cols]), f64(d["w"][cols]),
+                                            f64(d["b"][cols]), None, f64(d["dy"][..., cols]))
+    assert rel_err(y[..., cols], y_ref) <= FWD_TOL[BF]
+    assert rel_err(torch.cat(dxs, dim=1)[..., cols], dx_ref) <= BWD_TOL[BF]
+    assert rel_err(dw[cols], dw_ref) <= BWD_TOL[BF]
+    assert rel_err(db[cols], db_ref) <= BWD_TOL[BF]
