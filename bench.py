@@ -118,12 +118,6 @@ def kernel_model(name, dk, dv, esz=2, C=64):
         by = (C * (2 * dk + dv) * esz + C * f4 + dk * dv * esz + C * dv * esz
               + C * (3 * dk + dv) * esz + C * C * esz + C * f4 + dk * dv * esz + C * dv * esz)
         fl = 4 * C * dk * dv + 6 * C * dk * dv + 2 * C * C * dv
-    elif name == "tc_chain_recompute":
-        by = C * (2 * dk + dv) * esz + C * f4 + dk * dv * esz + C * dv * esz
-        fl = 4 * C * dk * dv
-    elif name == "tc_chain_bwd":
-        by = C * (3 * dk + dv) * esz + C * C * esz + C * f4 + dk * dv * esz + C * dv * esz
-        fl = 6 * C * dk * dv + 2 * C * C * dv
     elif name == "tc_grad":
         by = (C * (2 * dk + 2 * dv) * esz + C * esz + C * C * esz + C * f4 + 2 * dk * dv * esz
               + 2 * C * dv * esz + C * (2 * dk + dv) * esz + 2 * C * esz)

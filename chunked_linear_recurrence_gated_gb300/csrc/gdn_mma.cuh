@@ -81,16 +81,6 @@ __device__ __forceinline__ void lda_tr(uint32_t* a, const __nv_bfloat16* base, i
   ldsm_x4_t(smem_u32(base + krow * ld + mcol), a[0], a[1], a[2], a[3]);
 }
 
-// B fragments for two k16 steps of one n8 tile from storage [n][k] (row-major,
-// k contiguous): rows n in [n0, n0+8), k in [k0, k0+32). b[0..1] = k-step 0,
-// b[2..3] = k-step 1.
-__device__ __forceinline__ void ldb_nk_x2k(uint32_t* b, const __nv_bfloat16* base, int ld, int n0,
-                                           int k0) {
-  const int l = threadIdx.x & 31;
-  const __nv_bfloat16* p = base + (n0 + (l & 7)) * ld + k0 + (l >> 3) * 8;
-  ldsm_x4(smem_u32(p), b[0], b[1], b[2], b[3]);
-}
-
 // B fragments for one k16 step of two n8 tiles from storage [n][k]:
 // rows n in [n0, n0+16), k in [k0, k0+16). b[0..1] = tile n0, b[2..3] = tile n0+8.
 __device__ __forceinline__ void ldb_nk_x2n(uint32_t* b, const __nv_bfloat16* base, int ld, int n0,
@@ -121,10 +111,6 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
 }
 
 }  // namespace gdn
@@ -198,38 +184,6 @@ namespace gdn {
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
                : "memory");
-}
-}  // namespace gdn
-
-namespace gdn {
-// ---------------------------------------------------------------- thread-block clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-  return r;
-}
-// Cluster-wide barrier (all threads of all CTAs of the cluster).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
-                   : "memory");
-}
-// Arrive on the mbarrier at the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t rank) {
-  asm volatile(
-      "{\n .reg .b32 ra;\n mapa.shared::cluster.u32 ra, %0, %1;\n"
-      " mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n}\n" ::"r"(smem_u32(bar)),
-      "r"(rank)
-      : "memory");
-}
-// 1-D bulk copy global -> shared of every CTA in `mask` (same offsets), each
-// destination's mbarrier at the same offset receiving the transaction bytes.
-__device__ __forceinline__ void bulk_g2s_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                            uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1], %2, [%3], %4;\n" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
 }
 }  // namespace gdn
 

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
   for (int j = 0; j < 4; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e) aOV[j][e] = aWV[j][e] = 0.f;
-  float hd = 0.f, ybeta = 0.f;
+  float hd = 0.f;
 
   for (int c = 0; c < NCH; ++c) {
     if (c + 1 < NCH) {
@@ -276,7 +276,6 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
     }
     __syncthreads();  // this buffer is refilled two chunks later
   }
-  (void)ybeta;
   // block reduction of <dH, H_b>
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, off);
