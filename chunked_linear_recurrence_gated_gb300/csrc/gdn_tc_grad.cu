@@ -281,6 +281,10 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
   for (int off = 16; off > 0; off >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, off);
   if (l == 0) sm.red[w] = hd;
 
+  // this thread's two rows: per-row factors read once
+  const int rr[2] = {R0 + gq, R0 + gq + 8};
+  const float Gr[2] = {sG[rr[0]], sG[rr[1]]}, Dr[2] = {sdte[rr[0]], sdte[rr[1]]};
+  const float Br[2] = {sb[rr[0]], sb[rr[1]]}, gr_[2] = {sg[rr[0]], sg[rr[1]]};
   // ---- dQ = Gamma dOH ; dgamma += Gamma q . dOH ; dK = dte dKt ; rho = dte k . dKt
   float aQ[8][4], aK[8][4];
   {
@@ -288,18 +292,23 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = R0 + gq + 8 * (e >> 1), c = 64 * cw + 8 * j + 2 * tq + (e & 1);
-        const float qv = __bfloat162float(Bk.Q[r * LDK + c]);
-        const float kv = __bfloat162float(Bk.K[r * LDK + c]);
-        aQ[j][e] = sG[r] * aOH[j][e];
-        aK[j][e] = sdte[r] * aKt[j][e];
-        if (e < 2) {
-          pq0 += qv * aOH[j][e];
-          pk0 += kv * aKt[j][e];
+      for (int hf = 0; hf < 2; ++hf) {
+        const int r = rr[hf], c = 64 * cw + 8 * j + 2 * tq;
+        const float2 qv = unpack_bf16(*reinterpret_cast<const uint32_t*>(&Bk.Q[r * LDK + c]));
+        const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t*>(&Bk.K[r * LDK + c]));
+        const int e = 2 * hf;
+        aQ[j][e] = Gr[hf] * aOH[j][e];
+        aQ[j][e + 1] = Gr[hf] * aOH[j][e + 1];
+        aK[j][e] = Dr[hf] * aKt[j][e];
+        aK[j][e + 1] = Dr[hf] * aKt[j][e + 1];
+        const float pq = qv.x * aOH[j][e] + qv.y * aOH[j][e + 1];
+        const float pk = kv.x * aKt[j][e] + kv.y * aKt[j][e + 1];
+        if (hf == 0) {
+          pq0 += pq;
+          pk0 += pk;
         } else {
-          pq1 += qv * aOH[j][e];
-          pk1 += kv * aKt[j][e];
+          pq1 += pq;
+          pk1 += pk;
         }
       }
     pq0 = quad_reduce(pq0);
@@ -307,11 +316,10 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
     pk0 = quad_reduce(pk0);
     pk1 = quad_reduce(pk1);
     if (tq == 0) {
-      const int r0 = R0 + gq, r1 = R0 + gq + 8;
-      sm.rowacc[cw][r0] += sG[r0] * pq0;
-      sm.rowacc[cw][r1] += sG[r1] * pq1;
-      sm.rho[cw][r0] = sdte[r0] * pk0;
-      sm.rho[cw][r1] = sdte[r1] * pk1;
+      sm.rowacc[cw][rr[0]] += Gr[0] * pq0;
+      sm.rowacc[cw][rr[1]] += Gr[1] * pq1;
+      sm.rho[cw][rr[0]] = Dr[0] * pk0;
+      sm.rho[cw][rr[1]] = Dr[1] * pk1;
     }
     // HW -> smem (bf16)
 #pragma unroll
@@ -332,15 +340,18 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float cs0 = 0.f, cs1 = 0.f;
+      const int c = 32 * cw + 8 * j + 2 * tq;
+      const float2 gc = *reinterpret_cast<const float2*>(&sg[c]);
+      const float2 bc = *reinterpret_cast<const float2*>(&sb[c]);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int r = R0 + gq + 8 * hf, c = 32 * cw + 8 * j + 2 * tq;
+        const int r = rr[hf];
         const float2 qm = unpack_bf16(*reinterpret_cast<const uint32_t*>(qkm + r * LD64 + c));
         const float2 km = unpack_bf16(*reinterpret_cast<const uint32_t*>(kkm + r * LD64 + c));
         kk[j][2 * hf] = km.x;
         kk[j][2 * hf + 1] = km.y;
-        const float m0 = (c <= r) ? __expf(sg[r] - sg[c]) : 0.f;
-        const float m1 = (c + 1 <= r) ? __expf(sg[r] - sg[c + 1]) : 0.f;
+        const float m0 = (c <= r) ? __expf(gr_[hf] - gc.x) : 0.f;
+        const float m1 = (c + 1 <= r) ? __expf(gr_[hf] - gc.y) : 0.f;
         const float R0v = aOV[j][2 * hf] * qm.x, R1v = aOV[j][2 * hf + 1] * qm.y;
         if (hf == 0) rs0 += R0v + R1v; else rs1 += R0v + R1v;
         cs0 += R0v;
@@ -349,13 +360,12 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
         aOV[j][2 * hf + 1] *= m1;
         *reinterpret_cast<uint32_t*>(&late.P[r * LD64 + c]) =
             pack_bf16(aOV[j][2 * hf], aOV[j][2 * hf + 1]);
-        dT[j][2 * hf] = sb[c] * aWV[j][2 * hf];
-        dT[j][2 * hf + 1] = sb[c + 1] * aWV[j][2 * hf + 1];
+        dT[j][2 * hf] = bc.x * aWV[j][2 * hf];
+        dT[j][2 * hf + 1] = bc.y * aWV[j][2 * hf + 1];
       }
       cs0 = col_reduce(cs0);
       cs1 = col_reduce(cs1);
       if (gq == 0) {
-        const int c = 32 * cw + 8 * j + 2 * tq;
         sm.colacc[rw][c] += cs0;
         sm.colacc[rw][c + 1] += cs1;
       }
@@ -387,12 +397,16 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
       mma16816(hk[3], ah_, b1[2], b1[3]);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c = 32 * cw + 8 * j + 2 * tq + (e & 1);
-        dT[j][e] -= sb[c] * sG[c] * hk[j][e];
-      }
+    for (int j = 0; j < 4; ++j) {
+      const int c = 32 * cw + 8 * j + 2 * tq;
+      const float2 bc = *reinterpret_cast<const float2*>(&sb[c]);
+      const float2 Gc = *reinterpret_cast<const float2*>(&sG[c]);
+      const float f0 = bc.x * Gc.x, f1 = bc.y * Gc.y;
+      dT[j][0] -= f0 * hk[j][0];
+      dT[j][1] -= f1 * hk[j][1];
+      dT[j][2] -= f0 * hk[j][2];
+      dT[j][3] -= f1 * hk[j][3];
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -433,21 +447,23 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = R0 + gq + 8 * (e >> 1), c = 64 * cw + 8 * j + 2 * tq + (e & 1);
-        const float x = -xg[j][e];
-        aK[j][e] += sb[r] * sG[r] * x;
-        const float kx = x * __bfloat162float(Bk.K[r * LDK + c]);
-        if (e < 2) p0 += kx; else p1 += kx;
+      for (int hf = 0; hf < 2; ++hf) {
+        const int r = rr[hf], c = 64 * cw + 8 * j + 2 * tq;
+        const float bg = Br[hf] * Gr[hf];
+        const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t*>(&Bk.K[r * LDK + c]));
+        const float x0 = -xg[j][2 * hf], x1 = -xg[j][2 * hf + 1];
+        aK[j][2 * hf] += bg * x0;
+        aK[j][2 * hf + 1] += bg * x1;
+        const float kx = x0 * kv.x + x1 * kv.y;
+        if (hf == 0) p0 += kx; else p1 += kx;
       }
     p0 = quad_reduce(p0);
     p1 = quad_reduce(p1);
     if (tq == 0) {
-      const int r0 = R0 + gq, r1 = R0 + gq + 8;
-      sm.dbeta[cw][r0] += sG[r0] * p0;
-      sm.dbeta[cw][r1] += sG[r1] * p1;
-      sm.rowacc[cw][r0] += sb[r0] * sG[r0] * p0;
-      sm.rowacc[cw][r1] += sb[r1] * sG[r1] * p1;
+      sm.dbeta[cw][rr[0]] += Gr[0] * p0;
+      sm.dbeta[cw][rr[1]] += Gr[1] * p1;
+      sm.rowacc[cw][rr[0]] += Br[0] * Gr[0] * p0;
+      sm.rowacc[cw][rr[1]] += Br[1] * Gr[1] * p1;
     }
   }
   float z1[4][4];
@@ -497,13 +513,15 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float cg0 = 0.f, cg1 = 0.f;
+      const float2 gc = *reinterpret_cast<const float2*>(&sg[32 * cw + 8 * j + 2 * tq]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = R0 + gq + 8 * (e >> 1), c = 32 * cw + 8 * j + 2 * tq + (e & 1);
+        const int hf = e >> 1;
+        const int r = rr[hf], c = 32 * cw + 8 * j + 2 * tq + (e & 1);
         const float dA = (c < r) ? -da[j][e] : 0.f;
-        const float E = (c < r) ? dA * __expf(sg[r] - sg[c]) : 0.f;
+        const float E = (c < r) ? dA * __expf(gr_[hf] - ((e & 1) ? gc.y : gc.x)) : 0.f;
         const float dAK = dA * kk[j][e];  // dA * K K^T * Mask = E * K K^T
-        const float Gv = sb[r] * dAK;
+        const float Gv = Br[hf] * dAK;
         if (e < 2) {
           pb0 += dAK;
           rg0 += Gv;
@@ -512,7 +530,7 @@ __global__ void __launch_bounds__(256, 1) k_grad_tc(SeqMap m, const __nv_bfloat1
           rg1 += Gv;
         }
         if (e & 1) cg1 += Gv; else cg0 += Gv;
-        da[j][e] = sb[r] * E;
+        da[j][e] = Br[hf] * E;
       }
       cg0 = col_reduce(cg0);
       cg1 = col_reduce(cg1);
