@@ -258,12 +258,15 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
   __syncthreads();
   invert_unit_lower64<NT>(reinterpret_cast<const float*>(sm.Q), sm.Tf, sm.S);
   // Tw = T diag(beta Gamma), Tu = T diag(beta) (bf16); T itself for the backward
-  for (int idx = tid; idx < BT * BT; idx += NT) {
+  for (int idx = 2 * tid; idx < BT * BT; idx += 2 * NT) {  // column pairs
     const int r = idx >> 6, c = idx & 63;
-    const float t = sm.Tf[r * 68 + c];
-    sm.Tw[r * LD64 + c] = __float2bfloat16_rn(t * sm.b[c] * sm.G[c]);
-    sm.Tu[r * LD64 + c] = __float2bfloat16_rn(t * sm.b[c]);
-    if (ws.T) ws.T[bh * BT * BT + idx] = __float2bfloat16_rn(t);
+    const float2 t = *reinterpret_cast<const float2*>(&sm.Tf[r * 68 + c]);
+    const float2 bc = *reinterpret_cast<const float2*>(&sm.b[c]);
+    const float2 Gc = *reinterpret_cast<const float2*>(&sm.G[c]);
+    *reinterpret_cast<uint32_t*>(&sm.Tw[r * LD64 + c]) =
+        pack_bf16(t.x * bc.x * Gc.x, t.y * bc.y * Gc.y);
+    *reinterpret_cast<uint32_t*>(&sm.Tu[r * LD64 + c]) = pack_bf16(t.x * bc.x, t.y * bc.y);
+    if (ws.T) *reinterpret_cast<uint32_t*>(ws.T + bh * BT * BT + idx) = pack_bf16(t.x, t.y);
   }
   __syncthreads();
   // W = Tw K: rows [R0, R0 + 16), columns [64 cw, 64 cw + 64)
