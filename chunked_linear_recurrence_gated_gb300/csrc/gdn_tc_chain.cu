@@ -206,16 +206,25 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
       }
       // V^new^T = U^T - X^T
 #pragma unroll
-      for (int g = 0; g < RG; ++g)
+      for (int g = 0; g < RG; ++g) {
+        // U^T fragments at the accumulator positions (value rows, token pairs):
+        // a transposing matrix load of the token-major U tile, matrix 2j + hf
+        // = tokens [16w + 8j, +8) x values [8hf, +8)
+        uint32_t uf[4];
+        {
+          const int mi = l >> 3;
+          ldsm_x4_t(smem_u32(S.U + g * BT * LDU + (16 * w + 8 * (mi >> 1) + (l & 7)) * LDU +
+                             8 * (mi & 1)),
+                    uf[0], uf[1], uf[2], uf[3]);
+        }
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const int vr = 16 * g + gq + 8 * hf;
             const int t0 = 16 * w + 8 * j + 2 * tq;
-            const __nv_bfloat16* Ug = S.U + g * BT * LDU;
-            const float u0 = __bfloat162float(Ug[t0 * LDU + gq + 8 * hf]);
-            const float u1 = __bfloat162float(Ug[(t0 + 1) * LDU + gq + 8 * hf]);
+            const float2 uu = unpack_bf16(uf[2 * j + hf]);
+            const float u0 = uu.x, u1 = uu.y;
             const float v0 = u0 - (x[g][0][j][2 * hf] + x[g][1][j][2 * hf]);
             const float v1 = u1 - (x[g][0][j][2 * hf + 1] + x[g][1][j][2 * hf + 1]);
             const uint32_t pv = pack_bf16(v0, v1);
@@ -223,6 +232,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
             if (keep && ok)
               *reinterpret_cast<uint32_t*>(ws.VnT + bh * DV * BT + (size_t)(tile * BV + vr) * BT + t0) = pv;
           }
+      }
       // operands of the state update that do not depend on V^new: load before the barrier
       uint32_t bK[4][8], bM[4][4];
 #pragma unroll
