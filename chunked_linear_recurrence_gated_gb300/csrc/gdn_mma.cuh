@@ -150,8 +150,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // seconds of SM clock, sets *abort and returns false (the caller then skips its
 // work but keeps executing every barrier, so the kernel still terminates).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (*abort) return false;
-  if (mbar_try_wait(bar, parity)) return true;
+  const int aborted = *abort;  // read alongside the first try, not before it
+  const bool done = mbar_try_wait(bar, parity);
+  if (aborted) return false;
+  if (done) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort) return false;

@@ -460,7 +460,9 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
               *reinterpret_cast<const uint4*>(&sm.dHT[r * LDK + c]);
         }
       }
-      // dV^new^T for tokens [16w, 16w + 16): dO^T QKM + dH^T K~^T
+      // dV^new^T for tokens [16w, 16w + 16): dO^T QKM + dH^T K~^T; the dO^T
+      // fragments are kept for the dH update
+      uint32_t aO[RG][4][4];
       {
         uint32_t bK[DK / 16][4], bM[4][4];
 #pragma unroll
@@ -483,11 +485,11 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
             mma16816(a2[kc & 1][1], aD[kc], bK[kc][2], bK[kc][3]);
           }
 #pragma unroll
-          for (int kc = 0; kc < 4; ++kc) lda_tr(aD[kc], S.dO, LDO, 16 * g, 16 * kc);
+          for (int kc = 0; kc < 4; ++kc) lda_tr(aO[g][kc], S.dO, LDO, 16 * g, 16 * kc);
 #pragma unroll
           for (int kc = 0; kc < 4; ++kc) {
-            mma16816(a1[0], aD[kc], bM[kc][0], bM[kc][1]);
-            mma16816(a1[1], aD[kc], bM[kc][2], bM[kc][3]);
+            mma16816(a1[0], aO[g][kc], bM[kc][0], bM[kc][1]);
+            mma16816(a1[1], aO[g][kc], bM[kc][2], bM[kc][3]);
           }
 #pragma unroll
           for (int j = 0; j < 2; ++j)
@@ -526,16 +528,13 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
             dh[g][j][e] *= GC;
             d2[j][e] = 0.f;
           }
-        uint32_t aO[4][4], aV[4][4];
+        uint32_t aV[4][4];
 #pragma unroll
-        for (int kc = 0; kc < 4; ++kc) {
-          lda_tr(aO[kc], S.dO, LDO, 16 * g, 16 * kc);
-          lda_rm(aV[kc], sm.dVT, LD64, 16 * g, 16 * kc);
-        }
+        for (int kc = 0; kc < 4; ++kc) lda_rm(aV[kc], sm.dVT, LD64, 16 * g, 16 * kc);
 #pragma unroll
         for (int kc = 0; kc < 4; ++kc) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) mma16816(dh[g][j], aO[kc], bQ[kc][2 * j], bQ[kc][2 * j + 1]);
+          for (int j = 0; j < 4; ++j) mma16816(dh[g][j], aO[g][kc], bQ[kc][2 * j], bQ[kc][2 * j + 1]);
 #pragma unroll
           for (int j = 0; j < 4; ++j) mma16816(d2[j], aV[kc], bW[kc][2 * j], bW[kc][2 * j + 1]);
         }
