@@ -288,6 +288,30 @@ def time_steps(fn, K, dev):
     return s.elapsed_time(e)
 
 
+def gpu_local_cpus(dev_index):
+    """Host CPUs of the GPU's NUMA node (Linux sysfs via the PCI bus id), or None."""
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={dev_index}", "--query-gpu=pci.bus_id",
+                              "--format=csv,noheader"], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        dom, rest = out.split(":", 1)
+        bus = f"{int(dom, 16):04x}:{rest}".lower()
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return None
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return (node, cpus) if cpus else None
+    except Exception:
+        return None
+
+
 def e2e_measure(runner, K, dev):
     """Same step through the public API with host buffers: every chunk's inputs
     are copied in from pinned host memory and its results (o and every
@@ -296,6 +320,11 @@ def e2e_measure(runner, K, dev):
     a step starts only after the previous one has finished."""
     x = runner.x
     keys = ["q", "k", "v", "g", "beta", "do"]
+    # pinned buffers on the GPU's own NUMA node (the host link is the bound here)
+    saved_aff = os.sched_getaffinity(0)
+    local = gpu_local_cpus(dev.index if dev.index is not None else 0)
+    if local:
+        os.sched_setaffinity(0, local[1])
     host_in = {k: torch.empty(x[k].shape, dtype=x[k].dtype, pin_memory=True) for k in keys}
     for k in keys:
         host_in[k].copy_(x[k])
@@ -348,7 +377,8 @@ def e2e_measure(runner, K, dev):
 
     one()
     ms = time_steps(one, K, dev)
-    return ms / K, h2d, d2h
+    os.sched_setaffinity(0, saved_aff)
+    return ms / K, h2d, d2h, (local[0] if local else None)
 
 
 def conv_measure(K, warmup, dev, hbm, peak_kind):
@@ -583,11 +613,12 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        e_ms, h2d, d2h = e2e_measure(runner, max(1, min(args.steps, 3)), dev)
+        e_ms, h2d, d2h, node = e2e_measure(runner, max(1, min(args.steps, 3)), dev)
         e2e = {"value": tokens / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "copies": "pinned host buffers, per chunk on two copy streams overlapped "
-                         "with the kernels"}
+                         "with the kernels",
+               "host_numa_node": node}
     conv = None
     if not args.no_conv and not args.tokens:
         conv = conv_measure(max(3, min(args.steps, 10)), args.warmup, dev, hbm, peak_kind)
