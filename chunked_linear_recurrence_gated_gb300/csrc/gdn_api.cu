@@ -5,6 +5,7 @@
 #include "../../include/gdn.h"
 #include "../../include/gdn_profile.h"
 #include "gdn_internal.cuh"
+#include "gdn_mma.cuh"
 
 namespace gdn {
 
@@ -66,6 +67,22 @@ cudaError_t varlen_prep(const int* cu, int nseq, int T, int nblk_cap, int* blk0,
 }
 
 __global__ void k_status_ok(int* status) { status[0] = DEV_OK; }
+
+// Failure-detection self-check: one bounded wait on an mbarrier that never
+// completes (its one expected arrival never comes).
+__global__ void k_diag_wait(int* status, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&bar, 0, &abort, limit);
+  __syncthreads();
+  if (threadIdx.x == 0) status[0] = ok ? DEV_OK : DEV_TIMEOUT;
+}
 
 }  // namespace gdn
 
@@ -524,6 +541,13 @@ void gdn_profile_arm(void** events, int capacity) {
 }
 
 int gdn_profile_count(void) { return gdn::g_prof_n; }
+
+int gdn_diag_wait_timeout(void* workspace, int limit_log2, void* stream) {
+  if (!workspace || !al(workspace, kAlign)) return GDN_ERR_WORKSPACE;
+  const int lg = limit_log2 < 10 ? 10 : (limit_log2 > 32 ? 32 : limit_log2);
+  gdn::k_diag_wait<<<1, 32, 0, (cudaStream_t)stream>>>((int*)workspace, 1ll << lg);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
 
 const char* gdn_profile_name(int i) {
   return (i >= 0 && i < gdn::g_prof_n) ? gdn::g_prof_names[i] : nullptr;

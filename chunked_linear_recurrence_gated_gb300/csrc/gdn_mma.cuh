@@ -146,10 +146,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the barrier phase with the given parity. Gives up after about two
-// seconds of SM clock, sets *abort and returns false (the caller then skips its
-// work but keeps executing every barrier, so the kernel still terminates).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// Waits for the barrier phase with the given parity. Gives up after `limit` SM
+// clock cycles (default about two seconds), sets *abort and returns false (the
+// caller then skips its work but keeps executing every barrier, so the kernel
+// still terminates).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          long long limit = (1ll << 32)) {
   const int aborted = *abort;  // read alongside the first try, not before it
   const bool done = mbar_try_wait(bar, parity);
   if (aborted) return false;
@@ -157,7 +159,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort) return false;
-    if (clock64() - t0 > (1ll << 32)) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       return false;
     }

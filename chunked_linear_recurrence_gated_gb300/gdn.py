@@ -108,6 +108,8 @@ def load(build_if_missing: bool = False):
     lib.gdn_profile_arm.restype = None
     lib.gdn_profile_count.argtypes = []
     lib.gdn_profile_count.restype = I
+    lib.gdn_diag_wait_timeout.argtypes = [P, I, P]
+    lib.gdn_diag_wait_timeout.restype = I
     lib.gdn_profile_name.argtypes = [I]
     lib.gdn_profile_name.restype = ctypes.c_char_p
     _lib = lib
@@ -348,6 +350,12 @@ def gdn_conv_bwd(x, w, b, state_in, dy, dstate_out=None, act="silu", dx=None, dw
 
 def gdn_workspace_status(workspace, stream=None) -> int:
     return load().gdn_workspace_status(_p(workspace), _stream(stream))
+
+
+def diag_wait_timeout(workspace, limit_log2=20, stream=None) -> int:
+    """Runs the bounded-wait self-check (include/gdn_profile.h); read the
+    outcome with gdn_workspace_status."""
+    return load().gdn_diag_wait_timeout(_p(workspace), limit_log2, _stream(stream))
 
 
 def gdn_status_str(code: int) -> str:

@@ -28,6 +28,16 @@ void gdn_profile_arm(void** events, int capacity);
 int gdn_profile_count(void);
 const char* gdn_profile_name(int i);
 
+/* Self-check of the kernels' bounded waits (failure detection without a GPU
+ * fault). Launches one CTA that waits on an mbarrier nothing ever arrives at,
+ * through the same bounded wait the chain kernels use, with a limit of
+ * 2^limit_log2 SM clock cycles (clamped to [10, 32]); when the wait gives up
+ * the kernel records GDN_ERR_TIMEOUT in the workspace's status word and
+ * returns, leaving the context usable. Read the outcome with
+ * gdn_workspace_status. `workspace` is any gdn workspace (256-byte aligned).
+ * Returns GDN_ERR_WORKSPACE / GDN_ERR_CUDA on a bad pointer / failed launch. */
+int gdn_diag_wait_timeout(void* workspace, int limit_log2, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,8 +30,14 @@ def test_header_and_binding_agree():
 
 
 def test_library_exports_every_header_symbol(lib):
-    for name in header_functions() + header_functions("gdn_conv.h"):
+    for name in (header_functions() + header_functions("gdn_conv.h")
+                 + header_functions("gdn_profile.h")):
         assert hasattr(lib, name), name
+
+
+def test_diag_checks_workspace(lib):
+    assert lib.gdn_diag_wait_timeout(None, 20, None) == 3
+    assert lib.gdn_diag_wait_timeout(ctypes.c_void_p(FAKE + 16), 20, None) == 3
 
 
 def test_version_and_status_strings(lib):
