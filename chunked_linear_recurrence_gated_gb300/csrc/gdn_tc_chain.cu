@@ -160,14 +160,6 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
       const int tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
       const size_t bh = (size_t)(si.blk0 + lb) * H + h;
       const float* dec = S.dec;
-      if (keep && ok) {
-        __nv_bfloat16* Hg = ws.HbT + bh * DV * DK + (size_t)tile * BV * DK;
-        for (int idx = tid; idx < BV * 16; idx += 128) {
-          const int r = idx >> 4, c = (idx & 15) * 8;
-          *reinterpret_cast<uint4*>(Hg + r * DK + c) =
-              *reinterpret_cast<const uint4*>(&sm.HT[r * LDK + c]);
-        }
-      }
       // X^T = H^T W^T (W fragments shared by the row groups) and, forward, H^T Q~^T
       // from the same H^T fragments
       float x[RG][2][2][4], o1[RG][2][2][4];
@@ -202,6 +194,16 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
               mma16816(o1[g][kc & 1][1], aH[kc], bQ[2], bQ[3]);
             }
           }
+        }
+      }
+      // H_b for the gradient kernel (after the MMAs that read H^T were issued;
+      // H^T is rewritten only after the next barrier)
+      if (keep && ok) {
+        __nv_bfloat16* Hg = ws.HbT + bh * DV * DK + (size_t)tile * BV * DK;
+        for (int idx = tid; idx < BV * 16; idx += 128) {
+          const int r = idx >> 4, c = (idx & 15) * 8;
+          *reinterpret_cast<uint4*>(Hg + r * DK + c) =
+              *reinterpret_cast<const uint4*>(&sm.HT[r * LDK + c]);
         }
       }
       // V^new^T = U^T - X^T
@@ -451,15 +453,6 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
       const int lb = si.nblk - 1 - it;
       const size_t bh = (size_t)(si.blk0 + lb) * H + h;
       const float* dec = S.dec;
-      // dH_{b+1} (bf16, value-major) for the gradient kernel
-      if (ok) {
-        __nv_bfloat16* Dg = ws.dHT + bh * DV * DK + (size_t)tile * BV * DK;
-        for (int idx = tid; idx < BV * 16; idx += 128) {
-          const int r = idx >> 4, c = (idx & 15) * 8;
-          *reinterpret_cast<uint4*>(Dg + r * DK + c) =
-              *reinterpret_cast<const uint4*>(&sm.dHT[r * LDK + c]);
-        }
-      }
       // dV^new^T for tokens [16w, 16w + 16): dO^T QKM + dH^T K~^T; the dO^T
       // fragments are kept for the dH update
       uint32_t aO[RG][4][4];
@@ -504,6 +497,16 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
                 *reinterpret_cast<uint32_t*>(ws.dVnT + bh * DV * BT + (size_t)(tile * BV + vr) * BT + t0) =
                     pack_bf16(d0, d1);
             }
+        }
+      }
+      // dH_{b+1} (bf16, value-major) for the gradient kernel (dH^T is rewritten
+      // only after the next barrier)
+      if (ok) {
+        __nv_bfloat16* Dg = ws.dHT + bh * DV * DK + (size_t)tile * BV * DK;
+        for (int idx = tid; idx < BV * 16; idx += 128) {
+          const int r = idx >> 4, c = (idx & 15) * 8;
+          *reinterpret_cast<uint4*>(Dg + r * DK + c) =
+              *reinterpret_cast<const uint4*>(&sm.dHT[r * LDK + c]);
         }
       }
       // operands that do not depend on dV^new: load before the barrier
