@@ -1,8 +1,9 @@
 // Per-block gradient kernel of the bf16 tensor-core path: the reverse-mode
 // derivative of one block's Pre / ST / Out (StateFlow review, Eq. 2; the
 // backward rebuilds the trajectory Fwd consumed, Eq. 6) given H_b and V^new
-// from the recompute chain and dH_{b+1}, dV^new from the reverse chain (the
-// same steps as the oracle's chunkwise module).
+// from the recompute chain (or from the forward that kept them) and
+// dH_{b+1}, dV^new from the reverse chain (the same steps as the oracle's
+// chunkwise module).
 #include "gdn_internal.cuh"
 #include "gdn_mma.cuh"
 

@@ -7,10 +7,12 @@
 //         W = T diag(beta Gamma) K, U = T diag(beta) V, QKM = Q K^T * Mask
 //   ST  : V^new = U - W H_b ; H_{b+1} = Gamma_C H_b + K^T diag(e^{gamma_C - gamma}) V^new
 //   Out : O = diag(Gamma) Q H_b + QKM V^new
-// Pre also writes padded copies of the block's K and Q rows and the decay
-// factors (Gamma_r, e^{gamma_C - gamma_r}, gamma_r) so that the sequential
-// chains fetch every operand with one bulk copy. All contractions are
-// bf16 x bf16 -> fp32 warp-level MMAs; the triangular inverse is fp32.
+// Pre also writes padded, decay-scaled copies of the block's rows,
+// K~ = diag(e^{gamma_C - gamma}) K and Q~ = diag(e^{gamma}) Q, and the per-row
+// vectors (Gamma_r, e^{gamma_C - gamma_r}, gamma_r, beta_r), so that the
+// sequential chains fetch every operand with one bulk copy and scale nothing
+// but the state. All contractions are bf16 x bf16 -> fp32 warp-level MMAs;
+// the triangular inverse is fp32 with TF32 MMAs for its off-diagonal blocks.
 #include "gdn_internal.cuh"
 #include "gdn_mma.cuh"
 
