@@ -206,7 +206,9 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
               *reinterpret_cast<const uint4*>(&sm.HT[r * LDK + c]);
         }
       }
-      // V^new^T = U^T - X^T
+      // V^new^T = U^T - X^T (the forward keeps it in registers too and writes
+      // its global copy once the next phase's MMAs are issued)
+      uint32_t pvs[RG][2][2];
 #pragma unroll
       for (int g = 0; g < RG; ++g) {
         // U^T fragments at the accumulator positions (value rows, token pairs):
@@ -231,7 +233,9 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
             const float v1 = u1 - (x[g][0][j][2 * hf + 1] + x[g][1][j][2 * hf + 1]);
             const uint32_t pv = pack_bf16(v0, v1);
             *reinterpret_cast<uint32_t*>(&sm.VnT[vr * LD64 + t0]) = pv;
-            if (keep && ok)
+            if (MODE == CHAIN_FWD)
+              pvs[g][j][hf] = pv;
+            else if (ok)
               *reinterpret_cast<uint32_t*>(ws.VnT + bh * DV * BT + (size_t)(tile * BV + vr) * BT + t0) = pv;
           }
       }
@@ -266,6 +270,15 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
           float(*acc)[4] = (kc & 1) ? h2 : hs[g];
 #pragma unroll
           for (int j = 0; j < 4; ++j) mma16816(acc[j], aV[kc], bK[kc][2 * j], bK[kc][2 * j + 1]);
+        }
+        if (MODE == CHAIN_FWD && keep && ok) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+              *reinterpret_cast<uint32_t*>(ws.VnT + bh * DV * BT +
+                                           (size_t)(tile * BV + 16 * g + gq + 8 * hf) * BT +
+                                           16 * w + 8 * j + 2 * tq) = pvs[g][j][hf];
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
