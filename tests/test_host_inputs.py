@@ -45,3 +45,32 @@ def test_inputs_seeded_and_normalised():
     n = a["k"].float().norm(dim=-1)
     assert (n - 1).abs().max() < 1e-2
     assert (a["g"].float() < 0).all() and ((a["beta"].float() > 0) & (a["beta"].float() < 1)).all()
+
+
+def test_bench_models_every_compute_kernel_the_library_marks():
+    """Every compute kernel name the library's timing hook can report has a
+    design-bytes / flops model in bench.py (the dominant-kernel roofline needs
+    one), and the reference arm reports the GPU arm's workload config."""
+    import glob
+    import os
+    import re
+
+    import bench
+    from chunked_linear_recurrence_gated_gb300.inputs import workload
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    names = set()
+    for path in glob.glob(os.path.join(root, "chunked_linear_recurrence_gated_gb300", "csrc", "*.cu")):
+        text = open(path).read()
+        names |= set(re.findall(r'prof_mark\(st, "([a-z_0-9]+)"', text))
+        names |= set(re.findall(r'"(tc_[a-z_]+)" : "(?:tc_[a-z_]+)"', text))
+        names |= set(re.findall(r'"tc_[a-z_]+" : "(tc_[a-z_]+)"', text))
+    helpers = {"status", "varlen_prep", "conv_fwd", "conv_bwd", "conv_reduce"}
+    compute = sorted(names - helpers)
+    assert "tc_grad" in compute and "tc_chain_fwd_keep" in compute and "tc_chain_fwd" in compute
+    for name in compute:
+        model = bench.kernel_model(name, 128, 128)
+        assert model is not None and model[0] > 0, name
+    w = workload(bench.WORKLOAD_INDEX)
+    cfg = bench.workload_config(w, 1, False)
+    assert cfg["T"] == w.T and cfg["chunks"] == w.chunks and cfg["H"] == w.H
