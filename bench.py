@@ -613,14 +613,16 @@ def main():
 
     e2e = None
     if not args.no_e2e:
+        barrier(world)
         e_ms, h2d, d2h, node = e2e_measure(runner, max(1, min(args.steps, 3)), dev)
+        e_ms, _ = aggregate(e_ms, w.B * w.T, world, device=dev)  # slowest rank
         e2e = {"value": tokens / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "copies": "pinned host buffers, per chunk on two copy streams overlapped "
                          "with the kernels",
                "host_numa_node": node}
     conv = None
-    if not args.no_conv and not args.tokens:
+    if not args.no_conv and not args.tokens:  # per GPU (each rank its own sequence; rank 0 reports)
         conv = conv_measure(max(3, min(args.steps, 10)), args.warmup, dev, hbm, peak_kind)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
