@@ -129,6 +129,9 @@ def kernel_model(name, dk, dv, esz=2, C=64):
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi every 200 ms
+    while in context; the lines are kept in memory (or appended to
+    $GDN_CLOCKS_CSV when set)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -136,16 +139,23 @@ class ClockSampler:
     def __init__(self, device_index):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        self.lines = []
+        self.thread = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
 
     def __enter__(self):
+        import threading
+
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.f, stderr=subprocess.DEVNULL)
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -157,27 +167,30 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-            self.f.close()
+            self.thread.join(timeout=5)
+            out = os.environ.get("GDN_CLOCKS_CSV")
+            if out:
+                with open(out, "a") as f:
+                    f.writelines(self.lines)
         return False
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
+        if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for n, val in zip(names, parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(n)
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
