@@ -59,8 +59,9 @@
  * argument returns GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED /
  * GDN_ERR_WORKSPACE and leaves every buffer untouched. A launch failure
  * returns GDN_ERR_CUDA. Kernels never trap. Conditions that only the device
- * can see (a malformed cu_seqlens array) are recorded in a status word in the
- * workspace and the affected work is skipped; gdn_workspace_status reads it.
+ * can see (a malformed cu_seqlens array, a bounded wait that gave up) are
+ * recorded in a status word in the workspace and the affected work is
+ * skipped; gdn_workspace_status reads it.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -169,8 +170,9 @@ gdn_status gdn_varlen_bwd(const gdn_shape* shape, const int* cu_seqlens, int nse
  * library-owned device array of GDN_NOALLOC_SCRATCH_BYTES, held by every GPU
  * that loads the library until the process exits; a shape whose forward
  * workspace (gdn_chunk_workspace_bytes(shape, 0)) exceeds it is rejected with
- * GDN_ERR_WORKSPACE before anything is launched (for dk = dv = 128 bf16 that
- * is about 1600 blocks x heads, i.e. B * ceil(T / 64) * H <= 1600). The call
+ * GDN_ERR_WORKSPACE before anything is launched (for dk = dv = 128 bf16 the
+ * forward workspace is about 85 KiB per 64-token block and head, so the
+ * limit is B * ceil(T / 64) * H <= 771). The call
  * allocates nothing. Its first call on a device looks up the array's device
  * address on the current device; make that first call before any stream
  * capture. Every call on a device shares the one array and no part of it needs

@@ -178,3 +178,13 @@ def test_conv_host_checks(lib):
     assert lib.gdn_conv_bwd(ctypes.byref(s), *args, None, ws, None) == 3
     assert lib.gdn_conv_bwd(ctypes.byref(s), *args, P(FAKE), ws - 256, None) == 3
     assert lib.gdn_conv_bwd(ctypes.byref(s), *args, P(FAKE + 16), ws, None) == 3
+
+
+def test_noalloc_limit_matches_its_documentation(lib):
+    """The no-allocation forward accepts exactly the shapes whose forward
+    workspace fits GDN_NOALLOC_SCRATCH_BYTES (documented as 771 block-heads
+    at dk = dv = 128 bf16)."""
+    lim = 64 << 20
+    fits = lambda nbh: lib.gdn_chunk_workspace_bytes(
+        ctypes.byref(shape(B=1, T=64 * nbh, H=1)), 0) <= lim
+    assert fits(771) and not fits(772)
