@@ -271,6 +271,52 @@ class Runner:
         for i in reversed(range(n)):
             self.bwd_chunk(i)
 
+    def fwd_step(self):
+        for i in range(len(self.w.chunks)):
+            self.fwd_chunk(i)
+
+    def units(self):
+        """Token-heads of each call of one step (the units a launch processes)."""
+        return [self.w.B * int(L) * self.w.H for L in self.w.chunks]
+
+
+class VarlenRunner:
+    """The packed variable-length workload: one gdn_varlen_fwd and one
+    gdn_varlen_bwd call over all sequences (state restarts at every start)."""
+
+    def __init__(self, w, dev):
+        from chunked_linear_recurrence_gated_gb300 import gdn
+        from chunked_linear_recurrence_gated_gb300.inputs import cu_seqlens, make_workload_inputs
+
+        self.gdn = gdn
+        self.w = w
+        self.x = make_workload_inputs(w, device=dev)
+        self.cu = cu_seqlens(w.seqlens).to(dev)
+        nseq = len(w.seqlens)
+        self.o = torch.empty(1, w.T, w.H, w.dv, dtype=w.torch_dtype, device=dev)
+        self.Sf = torch.empty(nseq, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+        self.dS0 = torch.empty_like(self.Sf)
+        x = self.x
+        self.grads = (torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]),
+                      torch.empty_like(x["g"]), torch.empty_like(x["beta"]))
+        shp = gdn.shape_of(x["q"], x["v"])
+        self.ws_f = gdn.alloc_workspace(gdn.varlen_workspace_bytes(shp, nseq, False), dev)
+        self.ws_b = gdn.alloc_workspace(gdn.varlen_workspace_bytes(shp, nseq, True), dev)
+
+    def fwd_step(self):
+        x = self.x
+        self.gdn.gdn_varlen_fwd(self.cu, x["q"], x["k"], x["v"], x["g"], x["beta"], o=self.o,
+                                S_final=self.Sf, workspace=self.ws_f)
+
+    def step(self):
+        x = self.x
+        self.fwd_step()
+        self.gdn.gdn_varlen_bwd(self.cu, x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                                x["do"], grads=self.grads, dS0=self.dS0, workspace=self.ws_b)
+
+    def units(self):
+        return [self.w.T * self.w.H]
+
 
 def barrier(world):
     if world > 1:
@@ -454,7 +500,7 @@ def cpu_baseline(w, x, max_tokens=32768):
     """The oracle, as it stands, on a bounded sample: all heads of the first chunk."""
     import oracle
 
-    L = min(max_tokens, w.chunks[0])
+    L = min(max_tokens, w.chunks[0] if w.chunks else w.T)
     sub = {k: x[k][:, :L].float().cpu() for k in ("q", "k", "v", "g", "beta", "do")}
     threads = oracle.default_threads()
     t0 = time.perf_counter()
@@ -468,12 +514,109 @@ def cpu_baseline(w, x, max_tokens=32768):
 
 
 def workload_config(w, world, recompute):
-    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-            "chunks": w.chunks, "state": "fp32",
-            "backward": ("recomputes the Pre products" if recompute else
-                         "reads the Pre products its chunk's forward kept"),
-            "l2": "inputs larger than L2 (no flush)",
-            "parallelism": f"dp{world} (independent sequence per GPU)"}
+    cfg = {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+           "state": "fp32",
+           "backward": ("recomputes T / W / U and the per-block states from S_in "
+                        "(gdn_chunk_bwd)" if recompute else
+                        "reads the per-block products its chunk's forward kept "
+                        "(gdn_chunk_fwd_save / gdn_chunk_bwd_saved)"),
+           "l2": "inputs larger than L2 (no flush)",
+           "parallelism": f"dp{world} (independent sequence per GPU)"}
+    if w.seqlens is not None:
+        cfg["seqlens"] = len(w.seqlens)
+    else:
+        cfg["chunks"] = w.chunks
+    return cfg
+
+
+def op_roofline(w, ms, which="fwd+bwd"):
+    """The op's roofline for `which` (SURVEY 8(d) bytes / flops per token-head):
+    the slower of its algorithmic bytes at the measured HBM bandwidth and its
+    algorithmic flops at the measured bf16 tensor rate."""
+    hbm, bf16, _, _ = peaks()
+    fb, bb = alg_bytes_per_token_head(w.dk, w.dv)
+    ff, bf = alg_flops_per_token_head(w.dk, w.dv)
+    by, fl = (fb + bb, ff + bf) if which == "fwd+bwd" else (fb, ff)
+    th = w.B * w.T * w.H
+    t_bytes = by * th / (hbm * 1e9)
+    t_flops = fl * th / (bf16 * 1e12)
+    roof_ms = max(t_bytes, t_flops) * 1e3
+    return {"roofline_ms": roof_ms, "bound": "hbm" if t_bytes >= t_flops else "tensor",
+            "frac_of_roofline": roof_ms / ms,
+            "roofline_tokens_per_s": w.B * w.T / (roof_ms / 1e3)}
+
+
+# Which phase of the op each kernel belongs to: its roofline credits it with
+# that phase's algorithmic bytes (SURVEY 8(d)) for the token-heads it processes.
+KERNEL_PHASE = {"tc_grad": "bwd", "simt_grad": "bwd", "tc_chains_bwd": "bwd",
+                "tc_chain_rev": "bwd", "simt_st_bwd": "bwd"}
+
+
+def kernel_roofline(name, per_launch_ms, units_per_launch, w, hbm, peak_kind):
+    """Roofline of one kernel: SURVEY 8(d)'s algorithmic bytes per token-head of
+    the phase it serves (fwd: q, k, v, g, beta in, o out; bwd: q, k, v, g,
+    beta, do in, dq, dk, dv, dg, dbeta out) x the token-heads of each launch,
+    over the summed launch time."""
+    fb, bb = alg_bytes_per_token_head(w.dk, w.dv)
+    per_th = bb if KERNEL_PHASE.get(name, "fwd") == "bwd" else fb
+    alg = per_th * sum(units_per_launch)
+    t = sum(per_launch_ms) / 1e3
+    achieved = alg / t / 1e9
+    n = len(per_launch_ms)
+    launch_units = sum(units_per_launch) // max(n, 1)
+    traffic = measured_traffic(name) if launch_units == 32768 * 16 else None
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": traffic, "kernel": name,
+            "alg_bytes_per_launch": alg / max(n, 1), "launch_ms": sum(per_launch_ms) / max(n, 1),
+            "alg_bytes_per_token_head": per_th, "phase": KERNEL_PHASE.get(name, "fwd"),
+            "peak_source": peak_kind, "timing": "CUDA events on the launch stream"}
+
+
+def time_mode(runner, K, warmup, dev):
+    """ms per fwd+bwd step and per forward-only step of `runner` (CUDA events,
+    W warm-up steps first)."""
+    for _ in range(max(warmup, 3)):
+        runner.step()
+    torch.cuda.synchronize(dev)
+    ms = time_steps(runner.step, K, dev) / K
+    for _ in range(2):
+        runner.fwd_step()
+    ms_f = time_steps(runner.fwd_step, K, dev) / K
+    return ms, ms_f
+
+
+def per_kernel(runner, dev, nsteps=2):
+    """{kernel: [ms of each launch]} of `nsteps` instrumented steps."""
+    from chunked_linear_recurrence_gated_gb300 import gdn
+
+    timer = gdn.KernelTimer(capacity=4096)
+    with timer:
+        for _ in range(nsteps):
+            runner.step()
+    torch.cuda.synchronize(dev)
+    return timer.per_kernel()
+
+
+def other_workloads(dev, K, warmup):
+    """fwd and fwd+bwd tokens/s of the other bf16 workloads (mid 8K, hybrid
+    alpha = 0.5 with H 32, varlen with dv 256), recomputing backward, against
+    their op rooflines."""
+    from chunked_linear_recurrence_gated_gb300.inputs import workload
+
+    out = {}
+    for idx in (1, 3, 4):
+        w = workload(idx)
+        r = VarlenRunner(w, dev) if w.seqlens is not None else Runner(w, dev, reuse=False)
+        ms, ms_f = time_mode(r, K, warmup, dev)
+        out[w.name] = {"ms_per_step": ms, "tokens_per_s": w.B * w.T / (ms / 1e3),
+                       "frac_of_roofline": op_roofline(w, ms)["frac_of_roofline"],
+                       "fwd_ms": ms_f, "fwd_tokens_per_s": w.B * w.T / (ms_f / 1e3),
+                       "fwd_frac_of_roofline": op_roofline(w, ms_f, "fwd")["frac_of_roofline"],
+                       "api": "gdn_varlen_fwd/bwd" if w.seqlens is not None else
+                              f"gdn_chunk_fwd/bwd over {len(w.chunks)} chained chunks"}
+        del r
+        torch.cuda.empty_cache()
+    return out
 
 
 def reference_arm(args, w):
@@ -504,7 +647,7 @@ def reference_arm(args, w):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": dict(workload_config(w, args.gpus, args.recompute), sample_tokens=L,
+        "config": dict(workload_config(w, args.gpus, not args.kept), sample_tokens=L,
                        runs_on=f"host cores of rank 0 ({threads} threads)"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(threads, w.H),
                          "kind": "oracle", "sample": sample},
@@ -521,12 +664,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
-                    help="workload index (1-3: fixed-length chunked bf16 workloads)")
+                    help="workload index (1-3: fixed-length chunked bf16 workloads, "
+                         "4: packed varlen)")
     ap.add_argument("--no-conv", action="store_true",
                     help="skip the short-convolution measurement")
-    ap.add_argument("--recompute", action="store_true",
-                    help="backward recomputes the per-block Pre products instead of reading "
-                         "the ones its chunk's forward kept")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the summary of the other workloads")
+    ap.add_argument("--kept", action="store_true",
+                    help="headline on the backward that reads the products its chunk's "
+                         "forward kept instead of the recomputing backward")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run only the first N tokens (a whole number of chunks); "
                          "for small profiling cases")
@@ -537,7 +683,7 @@ def main():
     from chunked_linear_recurrence_gated_gb300.inputs import workload
 
     w = workload(args.workload)
-    if args.tokens:
+    if args.tokens and w.seqlens is None:
         n = 0
         acc = 0
         while n < len(w.chunks) and acc + w.chunks[n] <= args.tokens:
@@ -550,6 +696,7 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local = int(os.environ.get("LOCAL_RANK", 0))
+    recompute = not args.kept
 
     if args.impl == "reference":
         if rank == 0:
@@ -564,7 +711,8 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
 
-    runner = Runner(w, dev, reuse=not args.recompute)
+    varlen = w.seqlens is not None
+    runner = VarlenRunner(w, dev) if varlen else Runner(w, dev, reuse=not recompute)
     for _ in range(max(args.warmup, 3)):
         runner.step()
     barrier(world)
@@ -579,53 +727,41 @@ def main():
     barrier(world)
     ms_step, value = aggregate(ms / args.steps, w.B * w.T, world, device=dev)
     tokens = w.B * w.T * world
+    # forward alone (the same calls' first half)
+    for _ in range(2):
+        runner.fwd_step()
+    barrier(world)
+    ms_f = time_steps(runner.fwd_step, args.steps, dev)
+    ms_fwd, value_fwd = aggregate(ms_f / args.steps, w.B * w.T, world, device=dev)
 
     # per-kernel timing on the launch stream (instrumented replay of the same steps)
-    timer = gdn.KernelTimer(capacity=4096)
-    with timer:
-        for _ in range(min(2, args.steps)):
-            runner.step()
-    torch.cuda.synchronize(dev)
-    per = timer.per_kernel()
     nsteps_timed = min(2, args.steps)
+    per = per_kernel(runner, dev, nsteps_timed)
     launches = sum(len(v) for v in per.values()) // nsteps_timed
     totals = {k: sum(v) for k, v in per.items()}
     dom = max(totals, key=totals.get)
-    avg_ms = totals[dom] / len(per[dom])
     hbm, bf16, bf16_s, peak_kind = peaks()
-    nblk_heads = (max(w.chunks) // 64) * w.H  # block-heads in one launch of a chunk kernel
-    km = kernel_model(dom, w.dk, w.dv)
-    if km is not None:
-        by, fl = km
-        if dom.startswith("simt_"):
-            # fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock (2070 MHz)
-            alu_peak = 152 * 128 * 2 * 2.070e9 / 1e12
-            achieved = fl * nblk_heads / (avg_ms / 1e3) / 1e12
-            roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                    "frac": achieved / alu_peak, "traffic": None, "kernel": dom,
-                    "peak_source": "derived: fp32 FFMA lanes x max clock"}
-        else:
-            achieved = by * nblk_heads / (avg_ms / 1e3) / 1e9
-            traffic = measured_traffic(dom) if nblk_heads == 512 * 16 else None
-            roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "traffic": traffic, "kernel": dom,
-                    "alg_bytes_per_launch": by * nblk_heads, "launch_ms": avg_ms,
-                    "peak_source": peak_kind}
+    calls = runner.units() * nsteps_timed  # token-heads of each call, in order
+    nl = len(per[dom])
+    units = (calls * ((nl + len(calls) - 1) // len(calls)))[:nl] if nl != len(calls) else calls
+    if dom.startswith("simt_"):
+        # fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock (2070 MHz)
+        km = kernel_model(dom, w.dk, w.dv)
+        alu_peak = 152 * 128 * 2 * 2.070e9 / 1e12
+        achieved = km[1] * (sum(units) / 64) / (totals[dom] / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": achieved / alu_peak, "traffic": None, "kernel": dom,
+                "peak_source": "derived: fp32 FFMA lanes x max clock"}
     else:
-        roof = {"bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
-                "traffic": None, "kernel": dom}
-    fb, bb = alg_bytes_per_token_head(w.dk, w.dv)
-    ff, bf = alg_flops_per_token_head(w.dk, w.dv)
-    th = w.B * w.T * w.H
-    t_bytes = (fb + bb) * th / (hbm * 1e9)
-    t_flops = (ff + bf) * th / (bf16 * 1e12)
-    roof_ms = max(t_bytes, t_flops) * 1e3
-    op_roofline = {"roofline_ms": roof_ms, "bound": "hbm" if t_bytes >= t_flops else "tensor",
-                   "frac_of_roofline": roof_ms / ms_step,
-                   "roofline_tokens_per_s": w.B * w.T / (roof_ms / 1e3)}
+        roof = kernel_roofline(dom, per[dom], units, w, hbm, peak_kind)
+        km = kernel_model(dom, w.dk, w.dv)
+        if km is not None:
+            design = km[0] * sum(units) / 64 / (totals[dom] / 1e3) / 1e9
+            roof["design_bytes_per_launch"] = km[0] * sum(units) / 64 / nl
+            roof["design_frac"] = design / hbm
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not varlen:
         barrier(world)
         e_ms, h2d, d2h, node = e2e_measure(runner, max(1, min(args.steps, 3)), dev)
         e_ms, _ = aggregate(e_ms, w.B * w.T, world, device=dev)  # slowest rank
@@ -634,9 +770,25 @@ def main():
                "copies": "pinned host buffers, per chunk on two copy streams overlapped "
                          "with the kernels",
                "host_numa_node": node}
+    # the other backward of the same workload (kept products vs recomputing)
+    other = None
+    if not varlen:
+        alt = Runner(w, dev, reuse=recompute)
+        a_ms, a_ms_f = time_mode(alt, args.steps, args.warmup, dev)
+        a_ms, _ = aggregate(a_ms, w.B * w.T, world, device=dev)
+        a_per = per_kernel(alt, dev, nsteps_timed)
+        other = {"backward": workload_config(w, world, not recompute)["backward"],
+                 "ms_per_step": a_ms, "tokens_per_s": tokens / (a_ms / 1e3),
+                 "frac_of_roofline": op_roofline(w, a_ms)["frac_of_roofline"],
+                 "kernels_ms_per_step": {k: sum(v) / nsteps_timed for k, v in a_per.items()}}
+        del alt
+        torch.cuda.empty_cache()
     conv = None
-    if not args.no_conv and not args.tokens:  # per GPU (each rank its own sequence; rank 0 reports)
+    if not args.no_conv and not args.tokens and not varlen:
         conv = conv_measure(max(3, min(args.steps, 10)), args.warmup, dev, hbm, peak_kind)
+    others = None
+    if not args.no_others and not args.tokens and args.workload == WORKLOAD_INDEX:
+        others = other_workloads(dev, max(3, min(args.steps, 10)), args.warmup)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, runner.x)
@@ -647,13 +799,17 @@ def main():
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w, world, args.recompute),
+            "config": workload_config(w, world, recompute),
             "clocks": clk.summary(),
             "e2e": e2e,
             "gpu_launches": launches * args.steps,
             "roofline": roof,
-            "op_roofline": op_roofline,
+            "op_roofline": op_roofline(w, ms_step),
+            "fwd": {"value": value_fwd, "unit": UNIT, "ms_per_step": ms_fwd,
+                    "op_roofline": op_roofline(w, ms_fwd, "fwd")},
             "kernels_ms_per_step": {k: v / nsteps_timed for k, v in totals.items()},
+            "other_backward": other,
+            "other_workloads": others,
             "cpu_baseline": cpu,
             "short_conv": conv,
         }

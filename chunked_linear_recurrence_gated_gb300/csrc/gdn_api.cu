@@ -68,6 +68,12 @@ cudaError_t varlen_prep(const int* cu, int nseq, int T, int nblk_cap, int* blk0,
 
 __global__ void k_status_ok(int* status) { status[0] = DEV_OK; }
 
+cudaError_t reset_status(int* status, cudaStream_t st) {
+  prof_mark(st, "status");
+  k_status_ok<<<1, 1, 0, st>>>(status);
+  return cudaGetLastError();
+}
+
 // Failure-detection self-check: one bounded wait on an mbarrier that never
 // completes (its one expected arrival never comes).
 __global__ void k_diag_wait(int* status, long long limit) {
@@ -331,6 +337,9 @@ gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, c
     }
     if (p.varlen && (e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st)))
       return GDN_ERR_CUDA;
+    // the status word is cleared by the call's first kernel (the block-table
+    // kernel of a varlen call, else Pre); a call with no block runs no Pre
+    if (!p.varlen && p.nblk_cap == 0 && (e = reset_status(w.status, st))) return GDN_ERR_CUDA;
     const SeqMap m = make_map(p, cu, blk0, blk_seq);
     e = tc_fwd(m, p.dv, q, k, v, g, beta, S_in, o, S_out, w, st);
     return e ? GDN_ERR_CUDA : GDN_OK;
@@ -341,9 +350,7 @@ gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, c
   if (p.varlen)
     e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st);
   else {
-    prof_mark(st, "status");
-    k_status_ok<<<1, 1, 0, st>>>(w.status);
-    e = cudaGetLastError();
+    e = reset_status(w.status, st);
   }
   if (e) return GDN_ERR_CUDA;
   const SeqMap m = make_map(p, cu, blk0, blk_seq);
@@ -380,6 +387,10 @@ gdn_status run_bwd(const Plan& p, const int* cu, const void* q, const void* k, c
     if (saved) saved_layout(p, &w, (char*)saved);
     if (p.varlen && (e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st)))
       return GDN_ERR_CUDA;
+    // Pre clears the status word when it runs; the backward from kept
+    // products (or a call with no block) starts with the reverse chain instead
+    if (!p.varlen && (saved || p.nblk_cap == 0) && (e = reset_status(w.status, st)))
+      return GDN_ERR_CUDA;
     const SeqMap m = make_map(p, cu, blk0, blk_seq);
     e = tc_bwd(m, p.dv, q, k, v, g, beta, S_in, dout, dS_out, dq, dk, dv, dg, dbeta, dS_in, w,
                saved == nullptr, st);
@@ -390,9 +401,7 @@ gdn_status run_bwd(const Plan& p, const int* cu, const void* q, const void* k, c
   if (p.varlen)
     e = varlen_prep(cu, p.nseq, p.T, p.nblk_cap, blk0, blk_seq, w.status, st);
   else {
-    prof_mark(st, "status");
-    k_status_ok<<<1, 1, 0, st>>>(w.status);
-    e = cudaGetLastError();
+    e = reset_status(w.status, st);
   }
   if (e) return GDN_ERR_CUDA;
   const SeqMap m = make_map(p, cu, blk0, blk_seq);

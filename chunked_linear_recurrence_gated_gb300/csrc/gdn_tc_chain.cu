@@ -597,7 +597,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     k_chain_fwd(SeqMap m, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                 const float* S_in, float* S_out, __nv_bfloat16* __restrict__ o, TcWs ws) {
   extern __shared__ __align__(128) unsigned char smraw[];
-  if (m.cu == nullptr && blockIdx.x == 0 && threadIdx.x == 0) ws.status[0] = DEV_OK;
   chain_fwd_body<DV, CHAIN_FWD, 1>(m, blockIdx.x, q, k, S_in, S_out, o, ws, smraw);
 }
 
@@ -611,7 +610,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                  const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ dout,
                  const float* S_in, const float* dS_out, float* dS_in, TcWs ws) {
   extern __shared__ __align__(128) unsigned char smraw[];
-  if (m.cu == nullptr && blockIdx.x == 0 && threadIdx.x == 0) ws.status[0] = DEV_OK;
   if ((int)blockIdx.x < n)
     chain_fwd_body<DV, CHAIN_RECOMPUTE, BWD_RG>(m, blockIdx.x, q, k, S_in, nullptr, nullptr, ws,
                                                smraw);
@@ -627,7 +625,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                 const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ dout,
                 const float* dS_out, float* dS_in, TcWs ws) {
   extern __shared__ __align__(128) unsigned char smraw[];
-  if (m.cu == nullptr && blockIdx.x == 0 && threadIdx.x == 0) ws.status[0] = DEV_OK;
   chain_rev_body<DV, 1>(m, blockIdx.x, q, k, dout, dS_out, dS_in, ws, smraw);
 }
 

@@ -146,6 +146,10 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
   constexpr int NT = 256;
   BlockInfo bi;
   const int gb = blockIdx.x, h = blockIdx.y, H = m.H, tid = threadIdx.x;
+  // Pre is the first kernel of a fixed-length call: it clears the status word,
+  // which the later kernels of the call only ever set (varlen calls: the
+  // block-table kernel sets it)
+  if (m.cu == nullptr && gb == 0 && h == 0 && tid == 0) ws.status[0] = DEV_OK;
   if (!block_info(m, gb, bi)) return;
   extern __shared__ __align__(128) unsigned char smraw[];
   PreSmem<DV>& sm = *reinterpret_cast<PreSmem<DV>*>(smraw);

@@ -27,7 +27,7 @@ EXPORTS = ["gdn_chunk_workspace_bytes", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "gdn_varlen_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd",
            "gdn_status_str", "gdn_workspace_status", "gdn_path", "gdn_version",
            "gdn_chunk_fwd_noalloc", "gdn_chunk_saved_bytes", "gdn_chunk_fwd_save",
-           "gdn_chunk_bwd_saved"]
+           "gdn_chunk_bwd_saved", "gdn_noalloc_status"]
 GDN_WS_SAVED = 2
 # include/gdn_conv.h
 CONV_EXPORTS = ["gdn_conv_workspace_bytes", "gdn_conv_fwd", "gdn_conv_bwd"]
@@ -91,6 +91,10 @@ def load(build_if_missing: bool = False):
     lib.gdn_version.restype = I
     lib.gdn_chunk_fwd_noalloc.argtypes = [SP] + [P] * 8 + [P]
     lib.gdn_chunk_fwd_noalloc.restype = I
+    lib.gdn_noalloc_status.argtypes = [P]
+    lib.gdn_noalloc_status.restype = I
+    lib.gdn_diag_wait_timeout_noalloc.argtypes = [I, P]
+    lib.gdn_diag_wait_timeout_noalloc.restype = I
     lib.gdn_chunk_saved_bytes.argtypes = [SP]
     lib.gdn_chunk_saved_bytes.restype = Z
     lib.gdn_chunk_fwd_save.argtypes = [SP] + [P] * 8 + [P, Z, P, Z, P]
@@ -356,6 +360,16 @@ def diag_wait_timeout(workspace, limit_log2=20, stream=None) -> int:
     """Runs the bounded-wait self-check (include/gdn_profile.h); read the
     outcome with gdn_workspace_status."""
     return load().gdn_diag_wait_timeout(_p(workspace), limit_log2, _stream(stream))
+
+
+def gdn_noalloc_status(stream=None) -> int:
+    return load().gdn_noalloc_status(_stream(stream))
+
+
+def diag_wait_timeout_noalloc(limit_log2=20, stream=None) -> int:
+    """The bounded-wait self-check on the no-allocation forward's scratch;
+    read the outcome with gdn_noalloc_status."""
+    return load().gdn_diag_wait_timeout_noalloc(limit_log2, _stream(stream))
 
 
 def gdn_status_str(code: int) -> str:

@@ -61,7 +61,8 @@
  * returns GDN_ERR_CUDA. Kernels never trap. Conditions that only the device
  * can see (a malformed cu_seqlens array, a bounded wait that gave up) are
  * recorded in a status word in the workspace and the affected work is
- * skipped; gdn_workspace_status reads it.
+ * skipped; gdn_workspace_status reads it (gdn_noalloc_status for
+ * gdn_chunk_fwd_noalloc, whose status word sits in the library's scratch).
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -182,6 +183,15 @@ gdn_status gdn_varlen_bwd(const gdn_shape* shape, const int* cu_seqlens, int nse
 gdn_status gdn_chunk_fwd_noalloc(const gdn_shape* shape, const void* q, const void* k,
                                  const void* v, const void* g, const void* beta,
                                  const float* S_in, void* o, float* S_out, void* stream);
+
+/* The device-side status of gdn_chunk_fwd_noalloc calls on the current device
+ * (what gdn_workspace_status reports for a caller-provided workspace): a
+ * bounded wait that gave up inside the last call leaves GDN_ERR_TIMEOUT, and
+ * that call's outputs are then incomplete. Synchronises `stream`, returns the
+ * recorded status (GDN_OK if none) and resets it. Allocates nothing. The
+ * scratch array's device address is cached per device and context; it is
+ * looked up again after a device reset. */
+gdn_status gdn_noalloc_status(void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* gdn_status_str(gdn_status status);

@@ -38,6 +38,10 @@ const char* gdn_profile_name(int i);
  * Returns GDN_ERR_WORKSPACE / GDN_ERR_CUDA on a bad pointer / failed launch. */
 int gdn_diag_wait_timeout(void* workspace, int limit_log2, void* stream);
 
+/* The same self-check on the status word of gdn_chunk_fwd_noalloc's scratch
+ * on the current device; read the outcome with gdn_noalloc_status. */
+int gdn_diag_wait_timeout_noalloc(int limit_log2, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -71,6 +71,30 @@ def test_bench_models_every_compute_kernel_the_library_marks():
     for name in compute:
         model = bench.kernel_model(name, 128, 128)
         assert model is not None and model[0] > 0, name
+    # backward-phase kernels are credited with the backward's algorithmic bytes
+    for name in compute:
+        if "grad" in name or "rev" in name or "bwd" in name:
+            assert bench.KERNEL_PHASE.get(name) == "bwd", name
     w = workload(bench.WORKLOAD_INDEX)
     cfg = bench.workload_config(w, 1, False)
     assert cfg["T"] == w.T and cfg["chunks"] == w.chunks and cfg["H"] == w.H
+
+
+def test_bench_kernel_roofline_follows_the_survey_bytes():
+    """The dominant kernel's roofline counts SURVEY 8(d)'s algorithmic bytes
+    per token-head (fwd 4dk + 4dv + 4, bwd 8dk + 6dv + 8 at bf16) times the
+    token-heads of its launches, over the summed launch time."""
+    import bench
+    from chunked_linear_recurrence_gated_gb300.inputs import workload
+
+    w = workload(bench.WORKLOAD_INDEX)
+    assert bench.alg_bytes_per_token_head(128, 128) == (1028, 1800)
+    units = [32768 * 16] * 8
+    r = bench.kernel_roofline("tc_grad", [0.5] * 8, units, w, 1000.0, "test")
+    assert abs(r["achieved"] - 1800 * 32768 * 16 / 0.5e-3 / 1e9) < 1e-6
+    assert abs(r["frac"] - r["achieved"] / 1000.0) < 1e-12
+    r = bench.kernel_roofline("tc_pre", [0.5, 0.25], [100, 50], w, 1000.0, "test")
+    assert abs(r["achieved"] - 1028 * 150 / 0.75e-3 / 1e9) < 1e-6
+    # uneven launches: total units over total time, not the largest launch
+    r2 = bench.kernel_roofline("tc_grad", [1.0, 0.1], [1000, 100], w, 1000.0, "test")
+    assert abs(r2["achieved"] - 1800 * 1100 / 1.1e-3 / 1e9) < 1e-6

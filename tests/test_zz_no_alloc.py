@@ -62,3 +62,22 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     bad = gdn.gdn_shape(1, 64, 2, 96, 128, 1)
     rc = lib.gdn_chunk_fwd_noalloc(ctypes.byref(bad), *([fake] * 5), None, fake, None, None)
     assert rc == 2  # GDN_ERR_UNSUPPORTED, as gdn_chunk_fwd reports it
+
+
+def test_noalloc_status_reports_a_timeout_and_resets():
+    """The no-allocation forward's device status (a bounded wait that gave up)
+    is readable without a workspace pointer: the bounded-wait self-check on the
+    scratch's status word reports GDN_ERR_TIMEOUT through gdn_noalloc_status,
+    reading resets it, and the next call still computes correctly."""
+    assert gdn.gdn_noalloc_status() == 0
+    assert gdn.diag_wait_timeout_noalloc(limit_log2=20) == 0
+    assert gdn.gdn_noalloc_status() == 5  # GDN_ERR_TIMEOUT
+    assert gdn.gdn_noalloc_status() == 0
+    x = make_inputs(1, 200, 2, 128, 128, dtype=torch.bfloat16, seed=33, decay="weak",
+                    with_state=True)
+    d = {k: v.cuda() for k, v in x.items()}
+    o_ref, S_ref = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S_in"])
+    rc, o, S_out = call_noalloc(d, d["S_in"])
+    assert rc == 0
+    assert gdn.gdn_noalloc_status() == 0
+    assert torch.equal(o, o_ref) and torch.equal(S_out, S_ref)
