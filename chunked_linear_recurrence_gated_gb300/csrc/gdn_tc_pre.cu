@@ -11,10 +11,18 @@
 // K~ = diag(e^{gamma_C - gamma}) K and Q~ = diag(e^{gamma}) Q, and the per-row
 // vectors (Gamma_r, e^{gamma_C - gamma_r}, gamma_r, beta_r), so that the
 // sequential chains fetch every operand with one bulk copy and scale nothing
-// but the state. All contractions are bf16 x bf16 -> fp32 warp-level MMAs;
-// the triangular inverse is fp32 with TF32 MMAs for its off-diagonal blocks.
+// but the state.
+//
+// K K^T and Q K^T (64 x 64, reduced over the 128 keys) are warp-level MMAs
+// and the inverse is fp32 with TF32 MMAs for its off-diagonal blocks. W and U
+// are computed transposed, W^T = K^T (T diag(beta Gamma))^T and
+// U^T = V^T (T diag(beta))^T, so that their 128 rows (keys, values) fill a
+// tcgen05 MMA: one thread issues them from 128-byte-swizzled shared-memory
+// tiles into tensor memory, the warps read the rows back into shared-memory
+// tiles in the chains' layouts, and bulk copies store the tiles.
 #include "gdn_internal.cuh"
 #include "gdn_mma.cuh"
+#include "gdn_umma.cuh"
 
 namespace gdn {
 namespace {
@@ -24,20 +32,47 @@ constexpr int LD64 = TC_LD64;
 constexpr int LDU = TC_LDU;
 
 // ------------------------------------------------------------------ Pre
+// Shared memory (byte offsets from a 1024-aligned base). The swizzled K, Q
+// and V tiles hold rows t with 64-wide column tiles 8192 bytes apart. Once
+// the MMAs have read them, W [t][k] is staged in A's space and the
+// tile-major U at the start.
 template <int DV>
-struct PreSmem {
-  __nv_bfloat16 K[BT * LDK];
-  __nv_bfloat16 Q[BT * LDK];  // reused as the fp32 strictly-lower A (same size) after Q K^T
-  __nv_bfloat16 V[BT * (DV + 8)];
-  float Tf[BT * 68];          // T (fp32)
-  float S[16 * 52];           // block-row product of the inverse
-  __nv_bfloat16 Tw[BT * LD64];  // T diag(beta Gamma)
-  __nv_bfloat16 Tu[BT * LD64];  // T diag(beta)
-  float g[BT];
-  float b[BT];
-  float G[BT];
-  float dte[BT];
+struct PreLayout {
+  static constexpr uint32_t K = 0;                 // K (swizzled)
+  static constexpr uint32_t Q = 16384;             // Q (swizzled)
+  static constexpr uint32_t V = 32768;             // V (swizzled), DV / 64 tiles
+  static constexpr uint32_t A = V + DV * 128;      // fp32 A [64][68]; then W [64][LDK]
+  static constexpr uint32_t TF = A + 17408;        // fp32 T [64][68]
+  static constexpr uint32_t S = TF + 17408;        // fp32 [16][52] block-row product
+  static constexpr uint32_t TW = S + 4096;         // T diag(beta Gamma) [64][64] (swizzled)
+  static constexpr uint32_t TU = TW + 8192;        // T diag(beta) [64][64] (swizzled)
+  static constexpr uint32_t UST = 0;               // U, tile-major [DV/16][64][LDU]
+  static constexpr uint32_t VEC = TU + 8192;
+  static constexpr uint32_t BYTES = VEC + 4 * 256 + 64;
+  static constexpr uint32_t NCOL = 256;            // TMEM columns: W^T [0, 64), U^T [64, 64 + DV/2)
 };
+static_assert(PreLayout<128>::A % 1024 == 0 && PreLayout<128>::TW % 1024 == 0 &&
+                  PreLayout<128>::TU % 1024 == 0 && PreLayout<256>::A % 1024 == 0 &&
+                  PreLayout<256>::TW % 1024 == 0 && PreLayout<256>::TU % 1024 == 0,
+              "swizzled tiles start 1024-byte aligned");
+static_assert(PreLayout<128>::A >= (128 / 16) * BT * TC_LDU * 2 &&
+                  PreLayout<256>::A >= (256 / 16) * BT * TC_LDU * 2,
+              "the tile-major U fits below A");
+
+// Fragment loads of mma.m16n8k16 from a swizzled tile (64-wide column tiles
+// `tb` bytes apart): A rows [r0, r0+16) x cols [c0, c0+16); B for two n8
+// tiles from storage [n][k], rows n in [n0, n0+16), k in [k0, k0+16).
+__device__ __forceinline__ void lda_sw(uint32_t* a, uint32_t base, uint32_t tb, int r0, int c0) {
+  const int l = threadIdx.x & 31;
+  ldsm_x4(base + sw128(r0 + (l & 7) + ((l >> 3) & 1) * 8, c0 + (l >> 4) * 8, tb), a[0], a[1], a[2],
+          a[3]);
+}
+__device__ __forceinline__ void ldb_nk_sw(uint32_t* b, uint32_t base, uint32_t tb, int n0, int k0) {
+  const int l = threadIdx.x & 31;
+  const int mat = l >> 3;
+  ldsm_x4(base + sw128(n0 + (l & 7) + (mat >> 1) * 8, k0 + (mat & 1) * 8, tb), b[0], b[1], b[2],
+          b[3]);
+}
 
 // Inclusive prefix sum of the 64 values in sg (warp 0), fixed order.
 __device__ __forceinline__ void block_cumsum64(float* sg) {
@@ -132,18 +167,19 @@ __device__ void invert_unit_lower64(const float* A, float* Tf, float* S) {
   }
 }
 
-// 8 warps; warp (rw = w & 3, cw = w >> 2) owns rows [16 rw, 16 rw + 16) and
-// the cw-th half of the columns of every product.
+// 8 warps; for the warp-level products warp (rw = w & 3, cw = w >> 2) owns
+// rows [16 rw, 16 rw + 16) and the cw-th half of the columns; for the
+// tensor-memory read-back warp w owns lanes [32 (w & 3), +32) and the
+// (w >> 2)-th half of the columns.
 template <int DV>
-__global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16* __restrict__ q,
-                                                   const __nv_bfloat16* __restrict__ k,
-                                                   const __nv_bfloat16* __restrict__ v,
-                                                   const __nv_bfloat16* __restrict__ g,
-                                                   const __nv_bfloat16* __restrict__ beta,
-                                                   TcWs ws) {
+__global__ void __launch_bounds__(256, DV == 128 ? 2 : 1)
+    k_pre_tc(SeqMap m, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+             const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
+             const __nv_bfloat16* __restrict__ beta, TcWs ws) {
+  using L = PreLayout<DV>;
   constexpr int DK = 128;
-  constexpr int LDV = DV + 8;
   constexpr int NT = 256;
+  constexpr uint32_t TB = 8192;  // bytes between the 64-wide column tiles of K, Q, V
   BlockInfo bi;
   const int gb = blockIdx.x, h = blockIdx.y, H = m.H, tid = threadIdx.x;
   // Pre is the first kernel of a fixed-length call: it clears the status word,
@@ -151,65 +187,90 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
   // block-table kernel sets it)
   if (m.cu == nullptr && gb == 0 && h == 0 && tid == 0) ws.status[0] = DEV_OK;
   if (!block_info(m, gb, bi)) return;
-  extern __shared__ __align__(128) unsigned char smraw[];
-  PreSmem<DV>& sm = *reinterpret_cast<PreSmem<DV>*>(smraw);
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sb = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+  const uint32_t su = smem_u32(sb);
+  float* sA = reinterpret_cast<float*>(sb + L::A);
+  float* sTf = reinterpret_cast<float*>(sb + L::TF);
+  float* sS = reinterpret_cast<float*>(sb + L::S);
+  float* s_g = reinterpret_cast<float*>(sb + L::VEC);
+  float* s_b = s_g + BT;
+  float* s_G = s_b + BT;
+  float* s_dte = s_G + BT;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sb + L::VEC + 4 * 256);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sb + L::VEC + 4 * 256 + 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(sb + L::VEC + 4 * 256 + 16);
   const int w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
   const int rw = w & 3, cw = w >> 2, R0 = 16 * rw;
+  const int lq = w & 3, ch = w >> 2;  // TMEM lane quarter, column half
   const size_t bh = (size_t)gb * H + h;
 
   for (int idx = tid; idx < BT * (DK / 8); idx += NT) {
     const int r = idx >> 4, c = (idx & 15) * 8;
     const bool ok = r < bi.len;
     const size_t off = ((size_t)(bi.tok0 + (ok ? r : 0)) * H + h) * DK + c;
-    cp16(&sm.K[r * LDK + c], k + off, ok);
-    cp16(&sm.Q[r * LDK + c], q + off, ok);
+    cp16(sb + L::K + sw128(r, c, TB), k + off, ok);
+    cp16(sb + L::Q + sw128(r, c, TB), q + off, ok);
   }
   for (int idx = tid; idx < BT * (DV / 8); idx += NT) {
     const int r = idx / (DV / 8), c = (idx % (DV / 8)) * 8;
     const bool ok = r < bi.len;
-    cp16(&sm.V[r * LDV + c], v + ((size_t)(bi.tok0 + (ok ? r : 0)) * H + h) * DV + c, ok);
+    cp16(sb + L::V + (uint32_t)(c >> 6) * TB + sw128(r, c & 63, TB),
+         v + ((size_t)(bi.tok0 + (ok ? r : 0)) * H + h) * DV + c, ok);
   }
   cp_commit();
   if (tid < BT) {
     const bool ok = tid < bi.len;
     const size_t off = (size_t)(bi.tok0 + tid) * H + h;
-    sm.g[tid] = ok ? __bfloat162float(g[off]) : 0.f;
-    sm.b[tid] = ok ? __bfloat162float(beta[off]) : 0.f;
+    s_g[tid] = ok ? __bfloat162float(g[off]) : 0.f;
+    s_b[tid] = ok ? __bfloat162float(beta[off]) : 0.f;
   }
+  if (w == 0) tmem_alloc(tslot, L::NCOL);
+  if (tid == 0) {
+    mbar_init(mbar, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
   __syncthreads();
-  block_cumsum64(sm.g);
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  block_cumsum64(s_g);
   cp_wait<0>();
   __syncthreads();
   if (tid < BT) {
-    const float gr = sm.g[tid];
-    const float G = __expf(gr), dte = __expf(sm.g[BT - 1] - gr);
-    sm.G[tid] = G;
-    sm.dte[tid] = dte;
+    const float gr = s_g[tid];
+    const float G = __expf(gr), dte = __expf(s_g[BT - 1] - gr);
+    s_G[tid] = G;
+    s_dte[tid] = dte;
     float* dec = ws.dec + bh * TC_DEC_ROWS * BT;
     dec[tid] = G;
     dec[BT + tid] = dte;
     dec[2 * BT + tid] = gr;
-    dec[3 * BT + tid] = sm.b[tid];
+    dec[3 * BT + tid] = s_b[tid];
   }
   __syncthreads();
   // padded, decay-scaled copies for the chains (one bulk copy each per block):
-  // K~ = diag(e^{gamma_C - gamma}) K and Q~ = diag(e^{gamma}) Q
+  // K~ = diag(e^{gamma_C - gamma}) K and Q~ = diag(e^{gamma}) Q; the pad
+  // columns are written as zeros so every sector is written in full
   {
-    const uint4* sK = reinterpret_cast<const uint4*>(sm.K);
-    const uint4* sQ = reinterpret_cast<const uint4*>(sm.Q);
     uint4* gK = reinterpret_cast<uint4*>(ws.Kp + bh * BT * LDK);
     uint4* gQ = reinterpret_cast<uint4*>(ws.Qp + bh * BT * LDK);
-    for (int idx = tid; idx < BT * LDK / 8; idx += NT) {
-      const int r = idx / (LDK / 8);
-      const float sk = sm.dte[r], sq = sm.G[r];
-      uint4 a = sK[idx], b = sQ[idx];
-      uint32_t* pa = &a.x;
-      uint32_t* pb = &b.x;
+    for (int idx = tid; idx < BT * (LDK / 8); idx += NT) {
+      const int r = idx / (LDK / 8), c = (idx % (LDK / 8)) * 8;
+      uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+      if (c < DK) {
+        a = *reinterpret_cast<const uint4*>(sb + L::K + sw128(r, c, TB));
+        b = *reinterpret_cast<const uint4*>(sb + L::Q + sw128(r, c, TB));
+        const float sk = s_dte[r], sq = s_G[r];
+        uint32_t* pa = &a.x;
+        uint32_t* pb = &b.x;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 x = unpack_bf16(pa[e]), y = unpack_bf16(pb[e]);
-        pa[e] = pack_bf16(sk * x.x, sk * x.y);
-        pb[e] = pack_bf16(sq * y.x, sq * y.y);
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = unpack_bf16(pa[e]), y = unpack_bf16(pb[e]);
+          pa[e] = pack_bf16(sk * x.x, sk * x.y);
+          pb[e] = pack_bf16(sq * y.x, sq * y.y);
+        }
       }
       gK[idx] = a;
       gQ[idx] = b;
@@ -226,12 +287,12 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
 #pragma unroll
     for (int kc = 0; kc < DK / 16; ++kc) {
       uint32_t ak[4], aq[4];
-      lda_rm(ak, sm.K, LDK, R0, 16 * kc);
-      lda_rm(aq, sm.Q, LDK, R0, 16 * kc);
+      lda_sw(ak, su + L::K, TB, R0, 16 * kc);
+      lda_sw(aq, su + L::Q, TB, R0, 16 * kc);
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
         uint32_t b[4];
-        ldb_nk_x2n(b, sm.K, LDK, 32 * cw + 16 * jj, 16 * kc);
+        ldb_nk_sw(b, su + L::K, TB, 32 * cw + 16 * jj, 16 * kc);
         mma16816(kk[2 * jj], ak, b[0], b[1]);
         mma16816(kk[2 * jj + 1], ak, b[2], b[3]);
         mma16816(qk[2 * jj], aq, b[0], b[1]);
@@ -239,18 +300,16 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
       }
     }
     __nv_bfloat16* qkm = ws.QKM + bh * BT * LD64;
-    float* sA = reinterpret_cast<float*>(sm.Q);
-    __syncthreads();  // every warp is done reading Q before A overwrites it
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int r = R0 + gq + 8 * hf;
         const int c = 32 * cw + 8 * j + 2 * tq;
-        const float gr = sm.g[r];
-        const float d0 = (c <= r) ? __expf(gr - sm.g[c]) : 0.f;
-        const float d1 = (c + 1 <= r) ? __expf(gr - sm.g[c + 1]) : 0.f;
-        const float br = sm.b[r];
+        const float gr = s_g[r];
+        const float d0 = (c <= r) ? __expf(gr - s_g[c]) : 0.f;
+        const float d1 = (c + 1 <= r) ? __expf(gr - s_g[c + 1]) : 0.f;
+        const float br = s_b[r];
         const float km0 = (c < r) ? kk[j][2 * hf] * d0 : 0.f;
         const float km1 = (c + 1 < r) ? kk[j][2 * hf + 1] * d1 : 0.f;
         sA[r * 68 + c] = br * km0;
@@ -262,94 +321,90 @@ __global__ void __launch_bounds__(256, 2) k_pre_tc(SeqMap m, const __nv_bfloat16
       }
   }
   __syncthreads();
-  invert_unit_lower64<NT>(reinterpret_cast<const float*>(sm.Q), sm.Tf, sm.S);
-  // Tw = T diag(beta Gamma), Tu = T diag(beta) (bf16); T itself for the backward
+  invert_unit_lower64<NT>(sA, sTf, sS);
+  // Tw = T diag(beta Gamma), Tu = T diag(beta) as swizzled [t][j] tiles; T itself for the backward
   for (int idx = 2 * tid; idx < BT * BT; idx += 2 * NT) {  // column pairs
     const int r = idx >> 6, c = idx & 63;
-    const float2 t = *reinterpret_cast<const float2*>(&sm.Tf[r * 68 + c]);
-    const float2 bc = *reinterpret_cast<const float2*>(&sm.b[c]);
-    const float2 Gc = *reinterpret_cast<const float2*>(&sm.G[c]);
-    *reinterpret_cast<uint32_t*>(&sm.Tw[r * LD64 + c]) =
+    const float2 t = *reinterpret_cast<const float2*>(&sTf[r * 68 + c]);
+    const float2 bc = *reinterpret_cast<const float2*>(&s_b[c]);
+    const float2 Gc = *reinterpret_cast<const float2*>(&s_G[c]);
+    *reinterpret_cast<uint32_t*>(sb + L::TW + sw128(r, c, 0)) =
         pack_bf16(t.x * bc.x * Gc.x, t.y * bc.y * Gc.y);
-    *reinterpret_cast<uint32_t*>(&sm.Tu[r * LD64 + c]) = pack_bf16(t.x * bc.x, t.y * bc.y);
+    *reinterpret_cast<uint32_t*>(sb + L::TU + sw128(r, c, 0)) = pack_bf16(t.x * bc.x, t.y * bc.y);
     if (ws.T) *reinterpret_cast<uint32_t*>(ws.T + bh * BT * BT + idx) = pack_bf16(t.x, t.y);
   }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  // W = Tw K: rows [R0, R0 + 16), columns [64 cw, 64 cw + 64)
-  {
-    uint32_t at[4][4];
+
+  // W^T = K^T Tw^T -> TMEM columns [0, 64); U^T = V^T Tu^T -> [64, 64 + 64 DV/128)
+  if (tid == 0) {
+    tc_fence_after();
 #pragma unroll
-    for (int kc = 0; kc < 4; ++kc) lda_rm(at[kc], sm.Tw, LD64, R0, 16 * kc);
-    float acc[8][4];
+    for (int s = 0; s < 4; ++s) {
+      umma_bf16(tmem, umma_desc(su + L::K + 2048 * s, TB, 1024),
+                umma_desc(su + L::TW + 32 * s, 16, 1024), umma_idesc(128, 64, 1, 0), s > 0);
+      const uint64_t bu = umma_desc(su + L::TU + 32 * s, 16, 1024);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-#pragma unroll
-    for (int kc = 0; kc < 4; ++kc)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        uint32_t b[4];
-        ldb_kn_x2n(b, sm.K, LDK, 16 * kc, 64 * cw + 16 * jj);
-        mma16816(acc[2 * jj], at[kc], b[0], b[1]);
-        mma16816(acc[2 * jj + 1], at[kc], b[2], b[3]);
-      }
-    __nv_bfloat16* W = ws.W + bh * BT * LDK;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int r = R0 + gq + 8 * hf, c = 64 * cw + 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(W + r * LDK + c) = pack_bf16(acc[j][2 * hf], acc[j][2 * hf + 1]);
-      }
+      for (int mh = 0; mh < DV / 128; ++mh)
+        umma_bf16(tmem + 64 + 64 * mh, umma_desc(su + L::V + 2 * TB * mh + 2048 * s, TB, 1024), bu,
+                  umma_idesc(128, 64, 1, 0), s > 0);
+    }
+    umma_commit(mbar);
   }
-  // U = Tu V: rows [R0, R0 + 16), columns [DV/2 cw, DV/2 (cw + 1)), 64 at a time
-  {
-    uint32_t at[4][4];
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(mbar, 0, abort));  // warp-uniform for tcgen05.ld
+  tc_fence_after();
+  // read back: lane = key k (W^T) or value v (U^T), 32 tokens per warp; staged as
+  // W [t][k] (padded rows) in A's space and U tile-major at the start
+  if (ok) {
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
+    __nv_bfloat16* Wst = reinterpret_cast<__nv_bfloat16*>(sb + L::A);
+    __nv_bfloat16* Ust = reinterpret_cast<__nv_bfloat16*>(sb + L::UST);
 #pragma unroll
-    for (int kc = 0; kc < 4; ++kc) lda_rm(at[kc], sm.Tu, LD64, R0, 16 * kc);
-    __nv_bfloat16* U = ws.U + bh * (DV / 16) * BT * LDU;
+    for (int part = 0; part <= DV / 128; ++part) {
+      float vv[32];
+      tmem_ld16(lane_base + 64 * part + 32 * ch, vv);
+      tmem_ld16(lane_base + 64 * part + 32 * ch + 16, vv + 16);
+      if (part == 0) {
+        const int kk = 32 * lq + l;
 #pragma unroll
-    for (int c0 = 0; c0 < DV / 2; c0 += 64) {
-      const int cb = cw * (DV / 2) + c0;
-      float acc[8][4];
+        for (int i = 0; i < 32; ++i) Wst[(32 * ch + i) * LDK + kk] = __float2bfloat16_rn(vv[i]);
+      } else {
+        const int vv_ = 128 * (part - 1) + 32 * lq + l;
+        __nv_bfloat16* col = Ust + (size_t)(vv_ >> 4) * BT * LDU + (vv_ & 15);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-#pragma unroll
-      for (int kc = 0; kc < 4; ++kc)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          uint32_t b[4];
-          ldb_kn_x2n(b, sm.V, LDV, 16 * kc, cb + 16 * jj);
-          mma16816(acc[2 * jj], at[kc], b[0], b[1]);
-          mma16816(acc[2 * jj + 1], at[kc], b[2], b[3]);
-        }
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int r = R0 + gq + 8 * hf, c = cb + 8 * j + 2 * tq;
-          *reinterpret_cast<uint32_t*>(U + ((c >> 4) * BT + r) * LDU + (c & 15)) =
-              pack_bf16(acc[j][2 * hf], acc[j][2 * hf + 1]);
-        }
+        for (int i = 0; i < 32; ++i) col[(32 * ch + i) * LDU] = __float2bfloat16_rn(vv[i]);
+      }
+    }
+    // zero pad columns of the staged tiles
+    for (int r = tid; r < BT; r += NT)
+      *reinterpret_cast<uint4*>(Wst + r * LDK + DK) = make_uint4(0u, 0u, 0u, 0u);
+    for (int r = tid; r < (DV / 16) * BT; r += NT)
+      *reinterpret_cast<uint4*>(Ust + r * LDU + 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    if (ok) {
+      bulk_s2g(ws.W + bh * BT * LDK, sb + L::A, BT * LDK * 2);
+      bulk_s2g(ws.U + bh * (DV / 16) * BT * LDU, sb + L::UST, (DV / 16) * BT * LDU * 2);
+      bulk_commit();
+    } else {
+      ws.status[0] = DEV_TIMEOUT;
     }
   }
-  // zero the pad columns of the padded tiles: every 32-byte sector is then
-  // written in full, so none has to be read back from DRAM to merge it
+  // zero the pad columns of the other padded tiles
   {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    __nv_bfloat16* W = ws.W + bh * BT * LDK;
-    __nv_bfloat16* qkm = ws.QKM + bh * BT * LD64;
-    __nv_bfloat16* U = ws.U + bh * (DV / 16) * BT * LDU;
     for (int r = tid; r < BT; r += NT) {
-      *reinterpret_cast<uint4*>(W + r * LDK + DK) = z;
-      *reinterpret_cast<uint4*>(qkm + r * LD64 + BT) = z;
+      *reinterpret_cast<uint4*>(ws.QKM + bh * BT * LD64 + r * LD64 + BT) = z;
       if (ws.KKM) *reinterpret_cast<uint4*>(ws.KKM + bh * BT * LD64 + r * LD64 + BT) = z;
     }
-    for (int r = tid; r < (DV / 16) * BT; r += NT) *reinterpret_cast<uint4*>(U + r * LDU + 16) = z;
   }
+  if (tid == 0) bulk_wait_read();  // the staged tiles stay valid until read
+  __syncthreads();
+  if (w == 0) tmem_dealloc(tmem, L::NCOL);
 }
 
 template <class K>
@@ -362,10 +417,11 @@ cudaError_t launch_pre(const SeqMap& m, const void* q, const void* k, const void
                        const void* g, const void* beta, const TcWs& ws, cudaStream_t st) {
   using bf = __nv_bfloat16;
   cudaError_t e;
-  if ((e = set_smem(k_pre_tc<DV>, sizeof(PreSmem<DV>)))) return e;
+  constexpr size_t smem = PreLayout<DV>::BYTES + 1024;  // + alignment of the base
+  if ((e = set_smem(k_pre_tc<DV>, smem))) return e;
   if (m.nblk_cap > 0) {
     prof_mark(st, "tc_pre");
-    k_pre_tc<DV><<<dim3(m.nblk_cap, m.H), 256, sizeof(PreSmem<DV>), st>>>(
+    k_pre_tc<DV><<<dim3(m.nblk_cap, m.H), 256, smem, st>>>(
         m, (const bf*)q, (const bf*)k, (const bf*)v, (const bf*)g, (const bf*)beta, ws);
   }
   return cudaGetLastError();
