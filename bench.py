@@ -118,6 +118,10 @@ def kernel_model(name, dk, dv, esz=2, C=64):
         by = (C * (2 * dk + dv) * esz + C * f4 + dk * dv * esz + C * dv * esz
               + C * (3 * dk + dv) * esz + C * C * esz + C * f4 + dk * dv * esz + C * dv * esz)
         fl = 4 * C * dk * dv + 6 * C * dk * dv + 2 * C * C * dv
+    elif name == "tc_fwd_overlap":  # split forward: Pre and the forward chain, overlapped
+        by = (C * (2 * dk + dv) * esz + 2 * C * esz + C * (dk + dv) * esz + C * C * esz + C * f4
+              + C * (3 * dk + dv) * esz + C * C * esz + C * f4 + C * dv * esz)
+        fl = 4 * C * C * dk + C ** 3 / 3 + 2 * C * C * dk + 2 * C * C * dv + 6 * C * dk * dv + 2 * C * C * dv
     elif name == "tc_grad":
         by = (C * (2 * dk + 2 * dv) * esz + C * esz + C * C * esz + C * f4 + 2 * dk * dv * esz
               + 2 * C * dv * esz + C * (2 * dk + dv) * esz + 2 * C * esz)
@@ -597,6 +601,30 @@ def per_kernel(runner, dev, nsteps=2):
     return timer.per_kernel()
 
 
+SPLIT_SETTINGS = [(1, 0, 1), (1, 0, 2), (2, 0, 2), (4, 0, 2), (8, 0, 2), (16, 0, 2),
+                  (2, 300, 2), (2, 500, 2), (2, 700, 2), (2, 900, 2), (4, 0, 1)]
+
+
+def split_sweep(runner, K, dev):
+    """The forward with the chunk split into segments whose Pre kernel runs
+    beside the previous segment's state chain (the StateFlow review's
+    split-and-overlap of the state transition with the dense kernels): forward
+    ms per step for (segments, first segment's share f, 16-column groups per
+    chain CTA), against the serial order (1 segment)."""
+    from chunked_linear_recurrence_gated_gb300 import gdn
+
+    rows = []
+    for seg, pm, rg in SPLIT_SETTINGS:
+        gdn.set_fwd_split(seg, pm, rg)
+        for _ in range(2):
+            runner.fwd_step()
+        ms = time_steps(runner.fwd_step, K, dev) / K
+        rows.append({"segments": seg, "first_fraction": (pm / 1000) if pm else None,
+                     "chain_rg": rg, "fwd_ms": ms})
+    gdn.set_fwd_split(0, 0, 0)
+    return rows
+
+
 def other_workloads(dev, K, warmup):
     """fwd and fwd+bwd tokens/s of the other bf16 workloads (mid 8K, hybrid
     alpha = 0.5 with H 32, varlen with dv 256), recomputing backward, against
@@ -670,6 +698,8 @@ def main():
                     help="skip the short-convolution measurement")
     ap.add_argument("--no-others", action="store_true",
                     help="skip the summary of the other workloads")
+    ap.add_argument("--no-split-sweep", action="store_true",
+                    help="skip the split-forward (state-transition / dense overlap) sweep")
     ap.add_argument("--kept", action="store_true",
                     help="headline on the backward that reads the products its chunk's "
                          "forward kept instead of the recomputing backward")
@@ -733,6 +763,15 @@ def main():
     barrier(world)
     ms_f = time_steps(runner.fwd_step, args.steps, dev)
     ms_fwd, value_fwd = aggregate(ms_f / args.steps, w.B * w.T, world, device=dev)
+
+    # state-transition / dense-kernel overlap in the forward (split fraction sweep)
+    f2 = None
+    if not varlen and not args.no_split_sweep:
+        rows = split_sweep(runner, max(3, min(args.steps, 10)), dev)
+        serial = next(r["fwd_ms"] for r in rows if r["segments"] == 1 and r["chain_rg"] == 1)
+        best = min(rows, key=lambda r: r["fwd_ms"])
+        f2 = {"serial_fwd_ms": serial, "best": best, "best_gain_fwd_ms": serial - best["fwd_ms"],
+              "default_fwd_ms": ms_fwd, "settings": rows}
 
     # per-kernel timing on the launch stream (instrumented replay of the same steps)
     nsteps_timed = min(2, args.steps)
@@ -808,6 +847,7 @@ def main():
             "fwd": {"value": value_fwd, "unit": UNIT, "ms_per_step": ms_fwd,
                     "op_roofline": op_roofline(w, ms_fwd, "fwd")},
             "kernels_ms_per_step": {k: v / nsteps_timed for k, v in totals.items()},
+            "f2_overlap": f2,
             "other_backward": other,
             "other_workloads": others,
             "cpu_baseline": cpu,

@@ -248,6 +248,10 @@ size_t tc_layout(const Plan& p, int kind, TcWs* ws, int** blk0, int** blk_seq, c
     }
   }
   const bool states = kind == WS_BWD;  // WS_SAVED: H_b, V^new live with the saved products
+  // fp32 state between the segments of a split forward (forward workspaces)
+  const size_t sbytes = 4 * (size_t)p.nseq * p.H * p.dk * p.dv;
+  const size_t o_S0 = kind != WS_BWD ? c.take(sbytes) : 0;
+  const size_t o_S1 = kind != WS_BWD ? c.take(sbytes) : 0;
   size_t o_Hb = 0, o_Vn = 0, o_dH = 0, o_dVn = 0;
   if (states) {
     o_Hb = c.take(2 * nbh * p.dv * p.dk);
@@ -264,6 +268,8 @@ size_t tc_layout(const Plan& p, int kind, TcWs* ws, int** blk0, int** blk_seq, c
     ws->VnT = states ? (bf*)(base + o_Vn) : nullptr;
     ws->dHT = bwd ? (bf*)(base + o_dH) : nullptr;
     ws->dVnT = bwd ? (bf*)(base + o_dVn) : nullptr;
+    ws->Sseg[0] = kind != WS_BWD ? (float*)(base + o_S0) : nullptr;
+    ws->Sseg[1] = kind != WS_BWD ? (float*)(base + o_S1) : nullptr;
     *blk0 = p.varlen ? (int*)(base + o_blk0) : nullptr;
     *blk_seq = p.varlen ? (int*)(base + o_blks) : nullptr;
   }
@@ -310,11 +316,43 @@ SeqMap make_map(const Plan& p, const int* cu, const int* blk0, const int* blk_se
   return m;
 }
 
+// Split of a fixed-length tensor-core forward (state-transition / dense-kernel
+// overlap). The default is the setting measured fastest on the benchmark's
+// 32768-token chunks: no split (a chain CTA holds ~205 KB of shared memory, so
+// Pre cannot share its SMs, and a chain carrying 32 value columns per CTA to
+// leave SMs free runs 1.6x slower per step than the overlap gains);
+// gdn_diag_set_fwd_split overrides it for measurements.
+int g_split_nseg = 0;       // 0: default policy
+int g_split_permille = 0;   // first segment's share of the blocks when nseg = 2 (0: equal)
+int g_split_rg = 0;         // chain value-row groups (0: default)
+constexpr int kDefaultSegments = 1;
+constexpr int kDefaultSplitRG = 2;
+
+FwdSplit fwd_split(const Plan& p, bool allow) {
+  FwdSplit sp;
+  const int nblk = (p.T + BT - 1) / BT;
+  int nseg = g_split_nseg > 0 ? g_split_nseg : kDefaultSegments;
+  if (!allow || p.varlen) nseg = 1;
+  nseg = nseg < 1 ? 1 : (nseg > FwdSplit::kMaxSeg ? FwdSplit::kMaxSeg : nseg);
+  if (nseg > nblk) nseg = nblk > 0 ? nblk : 1;
+  sp.nseg = nseg;
+  sp.chain_rg = g_split_rg > 0 ? g_split_rg : (nseg > 1 ? kDefaultSplitRG : 1);
+  sp.b[0] = 0;
+  for (int i = 1; i < nseg; ++i) sp.b[i] = (int)(((long long)nblk * i) / nseg);
+  if (nseg == 2 && g_split_permille > 0) {
+    int b1 = (int)(((long long)nblk * g_split_permille + 500) / 1000);
+    sp.b[1] = b1 < 1 ? 1 : (b1 > nblk - 1 ? nblk - 1 : b1);
+  }
+  sp.b[nseg] = nblk;
+  return sp;
+}
+
 // `saved` (nullable): the forward also keeps its Pre products there, with the
 // backward's T and K K^T tiles, for run_bwd to read instead of recomputing.
 gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, void* o, float* S_out,
-                   void* saved, size_t savedb, void* ws, size_t wsb, void* stream) {
+                   void* saved, size_t savedb, void* ws, size_t wsb, void* stream,
+                   bool allow_split = true) {
   const size_t esz = p.dtype == GDN_DTYPE_F32 ? 4 : 2;
   const bool any = p.T > 0;
   if (!check_tensor(q, any, 16) || !check_tensor(k, any, 16) || !check_tensor(v, any, 16) ||
@@ -341,7 +379,7 @@ gdn_status run_fwd(const Plan& p, const int* cu, const void* q, const void* k, c
     // kernel of a varlen call, else Pre); a call with no block runs no Pre
     if (!p.varlen && p.nblk_cap == 0 && (e = reset_status(w.status, st))) return GDN_ERR_CUDA;
     const SeqMap m = make_map(p, cu, blk0, blk_seq);
-    e = tc_fwd(m, p.dv, q, k, v, g, beta, S_in, o, S_out, w, st);
+    e = tc_fwd(m, p.dv, q, k, v, g, beta, S_in, o, S_out, w, fwd_split(p, allow_split), st);
     return e ? GDN_ERR_CUDA : GDN_OK;
   }
   SimtWs w;
@@ -412,7 +450,27 @@ gdn_status run_bwd(const Plan& p, const int* cu, const void* q, const void* k, c
 
 }  // namespace
 
+namespace gdn {
+// gdn_chunk_fwd without the split forward (which creates internal streams on
+// first use): the no-allocation entry point's forward.
+gdn_status chunk_fwd_unsplit(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                             const void* g, const void* beta, const float* S_in, void* o,
+                             float* S_out, void* workspace, size_t workspace_bytes, void* stream) {
+  Plan p;
+  gdn_status s = plan_shape(shape, false, 0, &p);
+  if (s != GDN_OK) return s;
+  return run_fwd(p, nullptr, q, k, v, g, beta, S_in, o, S_out, nullptr, 0, workspace,
+                 workspace_bytes, stream, false);
+}
+}  // namespace gdn
+
 extern "C" {
+
+void gdn_diag_set_fwd_split(int segments, int first_permille, int chain_rg) {
+  g_split_nseg = segments > 0 ? segments : 0;
+  g_split_permille = first_permille > 0 && first_permille < 1000 ? first_permille : 0;
+  g_split_rg = chain_rg == 1 || chain_rg == 2 ? chain_rg : 0;
+}
 
 size_t gdn_chunk_workspace_bytes(const gdn_shape* shape, int is_bwd) {
   Plan p;

@@ -105,6 +105,18 @@ struct TcWs {
   __nv_bfloat16* VnT;    // [nblk, H, dv, BT]      V^new^T             (backward)
   __nv_bfloat16* dHT;    // [nblk, H, dv, 128]     dH_{b+1}^T          (backward)
   __nv_bfloat16* dVnT;   // [nblk, H, dv, BT]      dV^new^T            (backward)
+  float* Sseg[2];        // [B, H, dk, dv] x 2     fp32 state between the segments of a split forward
+};
+
+// How a fixed-length forward call is carried out: nseg = 1 runs Pre over
+// the whole chunk, then the chain; nseg > 1 splits the chunk's blocks at
+// b[1..nseg-1] (64-token boundaries) and overlaps Pre of one segment with the
+// chain of the previous one. chain_rg = value-row groups of 16 per chain CTA.
+struct FwdSplit {
+  static constexpr int kMaxSeg = 16;
+  int nseg = 1;
+  int chain_rg = 1;
+  int b[kMaxSeg + 1] = {};
 };
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }

@@ -17,8 +17,11 @@ cudaError_t simt_bwd(const SeqMap& m, int dk, int dv, int dtype, const void* q, 
 
 // bf16 tensor-core kernels; dk = 128, dv in {128, 256}.
 // Pre (gdn_tc_pre.cu): W, U, QKM, padded K / Q, decay factors, T.
+// nb > 0: only blocks [b0, b0 + nb) of each sequence (fixed-length calls).
+// mark: record the kernel with the timing hook.
 cudaError_t tc_pre(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
-                   const void* g, const void* beta, const TcWs& ws, cudaStream_t st);
+                   const void* g, const void* beta, const TcWs& ws, int b0, int nb,
+                   cudaStream_t st, bool mark);
 // Per-block gradients (gdn_tc_grad.cu).
 cudaError_t tc_grad(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
                     const void* beta, const void* dout, void* dq, void* dk_out, void* dv_out,
@@ -28,7 +31,7 @@ cudaError_t tc_grad(const SeqMap& m, int dv, const void* q, const void* k, const
 // K K^T) that a forward call wrote for the same inputs.
 cudaError_t tc_fwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, void* o, float* S_out,
-                   const TcWs& ws, cudaStream_t st);
+                   const TcWs& ws, const FwdSplit& sp, cudaStream_t st);
 cudaError_t tc_bwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, const void* dout,
                    const float* dS_out, void* dq, void* dk_out, void* dv_out, void* dg,

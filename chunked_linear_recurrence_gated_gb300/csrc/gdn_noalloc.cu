@@ -73,6 +73,12 @@ gdn_status scratch_for_current_device(void** out) {
 
 }  // namespace
 
+namespace gdn {
+gdn_status chunk_fwd_unsplit(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                             const void* g, const void* beta, const float* S_in, void* o,
+                             float* S_out, void* workspace, size_t workspace_bytes, void* stream);
+}
+
 extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_shape* shape, const void* q, const void* k,
                                             const void* v, const void* g, const void* beta,
                                             const float* S_in, void* o, float* S_out,
@@ -84,8 +90,8 @@ extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_shape* shape, const void* 
   void* scratch = nullptr;
   const gdn_status s = scratch_for_current_device(&scratch);
   if (s != GDN_OK) return s;
-  return gdn_chunk_fwd(shape, q, k, v, g, beta, S_in, o, S_out, scratch,
-                       (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream);
+  return gdn::chunk_fwd_unsplit(shape, q, k, v, g, beta, S_in, o, S_out, scratch,
+                                (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 extern "C" gdn_status gdn_noalloc_status(void* stream) {

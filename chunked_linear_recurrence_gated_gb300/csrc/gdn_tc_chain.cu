@@ -21,6 +21,8 @@
 //   dV^new = QKM^T dO + K~ dH ;  dH <- Gamma_C dH + Q~^T dO - W^T dV^new
 // The backward call runs the recompute chain (which rebuilds H_b and V^new
 // from S_in) and the reverse chain concurrently: they depend only on Pre.
+#include <mutex>
+
 #include "gdn_internal.cuh"
 #include "gdn_mma.cuh"
 
@@ -34,6 +36,38 @@ constexpr int DK = 128;
 constexpr int CHAIN_THREADS = 160;  // 4 compute warps + 1 producer warp
 
 enum { CHAIN_FWD = 0, CHAIN_RECOMPUTE = 1 };
+
+// Internal streams of the split forward (created once per device): Pre on
+// the lowest priority, the chain on the highest, so the chain's CTAs take
+// SMs first and Pre fills the rest. Calls that split share them: the host
+// side of a split call holds the device's lock while it enqueues.
+struct SideStreams {
+  std::mutex mu;
+  cudaStream_t pre = nullptr, chain = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, seg[FwdSplit::kMaxSeg] = {};
+};
+
+SideStreams* side_streams() {
+  static std::mutex init_mu;
+  static SideStreams* per_dev[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(init_mu);
+  if (!per_dev[dev]) {
+    SideStreams* ss = new SideStreams();
+    int least = 0, greatest = 0;
+    bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
+              cudaStreamCreateWithPriority(&ss->pre, cudaStreamNonBlocking, least) == cudaSuccess &&
+              cudaStreamCreateWithPriority(&ss->chain, cudaStreamNonBlocking, greatest) == cudaSuccess &&
+              cudaEventCreateWithFlags(&ss->fork, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&ss->join, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < FwdSplit::kMaxSeg; ++i)
+      ok = cudaEventCreateWithFlags(&ss->seg[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return nullptr;  // (the handles stay with the process; no call uses them)
+    per_dev[dev] = ss;
+  }
+  return per_dev[dev];
+}
 
 // ------------------------------------------------------------------ forward / recompute
 template <int MODE, int RG>
@@ -62,13 +96,17 @@ struct FwdSmem {
   int abort;
 };
 
+// Blocks [lb0, min(lb1, nblk)) of each sequence: the whole sequence, or one
+// segment of a split forward call (the state enters from S_in and leaves
+// through S_out, both exact fp32).
 template <int DV, int MODE, int RG>
 __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
                                                const __nv_bfloat16* __restrict__ q,
                                                const __nv_bfloat16* __restrict__ k,
                                                const float* S_in, float* S_out,
                                                __nv_bfloat16* __restrict__ o, const TcWs& ws,
-                                               unsigned char* smraw) {
+                                               unsigned char* smraw, int lb0 = 0,
+                                               int lb1 = 1 << 30) {
   constexpr int BV = 16 * RG;
   constexpr int NVT = DV / BV;
   constexpr int NS = fwd_stages<MODE, RG>();
@@ -78,6 +116,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
   const int H = m.H, h = sh % H, s = sh / H;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
   const SeqInfo si = seq_info(m, s);
+  const int nb = max(0, min(si.nblk, lb1) - lb0);  // blocks this launch carries
   FwdSmem<MODE, RG>& sm = *reinterpret_cast<FwdSmem<MODE, RG>*>(smraw);
   volatile int* abort = &sm.abort;
   // H_b and V^new of every block go to the workspace for the gradient kernel:
@@ -122,9 +161,10 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
   if (w == 4) {
     // ---------------- producer warp
     int issued = 0;
-    for (int lb = 0; lb < si.nblk; ++lb) {
-      const int st = lb % NS, kf = lb / NS;
-      if (lb >= NS && !mbar_wait(&sm.empty[st], (kf - 1) & 1, abort)) break;
+    for (int i = 0; i < nb; ++i) {
+      const int lb = lb0 + i;
+      const int st = i % NS, kf = i / NS;
+      if (i >= NS && !mbar_wait(&sm.empty[st], (kf - 1) & 1, abort)) break;
       FwdStage<MODE, RG>& S = sm.st[st];
       const size_t bh = (size_t)(si.blk0 + lb) * H + h;
       const uint32_t bytes = 2 * BT * LDK * 2 + RG * BT * LDU * 2 + 3 * BT * 4 +
@@ -145,17 +185,18 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
     }
     __syncwarp();
     if (*abort && l == 0) {  // after a timeout: let every copy still in flight land
-      for (int lb = max(0, issued - NS); lb < issued; ++lb) {
+      for (int i = max(0, issued - NS); i < issued; ++i) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(&sm.full[lb % NS], (lb / NS) & 1) && clock64() - t0 < (1ll << 31)) {
+        while (!mbar_try_wait(&sm.full[i % NS], (i / NS) & 1) && clock64() - t0 < (1ll << 31)) {
         }
       }
     }
   } else {
     // ---------------- compute warps
-    for (int lb = 0; lb < si.nblk; ++lb) {
-      const int st = lb % NS;
-      const bool ok = mbar_wait(&sm.full[st], (lb / NS) & 1, abort);
+    for (int i = 0; i < nb; ++i) {
+      const int lb = lb0 + i;
+      const int st = i % NS;
+      const bool ok = mbar_wait(&sm.full[st], (i / NS) & 1, abort);
       const FwdStage<MODE, RG>& S = sm.st[st];
       const int tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
       const size_t bh = (size_t)(si.blk0 + lb) * H + h;
@@ -592,12 +633,13 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
 // Forward: 16 value columns per CTA (the most SMs per head: the chain step is
 // bounded by each CTA's shared-memory traffic, which does not shrink with fewer
 // columns per CTA).
-template <int DV>
+template <int DV, int RG>
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     k_chain_fwd(SeqMap m, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                const float* S_in, float* S_out, __nv_bfloat16* __restrict__ o, TcWs ws) {
+                const float* S_in, float* S_out, __nv_bfloat16* __restrict__ o, TcWs ws, int lb0,
+                int lb1) {
   extern __shared__ __align__(128) unsigned char smraw[];
-  chain_fwd_body<DV, CHAIN_FWD, 1>(m, blockIdx.x, q, k, S_in, S_out, o, ws, smraw);
+  chain_fwd_body<DV, CHAIN_FWD, RG>(m, blockIdx.x, q, k, S_in, S_out, o, ws, smraw, lb0, lb1);
 }
 
 // Backward: the recompute chain (CTAs [0, n)) and the reverse chain (CTAs
@@ -633,20 +675,61 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+template <int DV, int RG>
+cudaError_t launch_chain_fwd(const SeqMap& m, const void* q, const void* k, const float* S_in,
+                             void* o, float* S_out, const TcWs& ws, int lb0, int lb1,
+                             cudaStream_t st, bool mark) {
+  using bf = __nv_bfloat16;
+  constexpr size_t smem = sizeof(FwdSmem<CHAIN_FWD, RG>);
+  cudaError_t e;
+  if ((e = set_smem(k_chain_fwd<DV, RG>, smem))) return e;
+  if (mark) prof_mark(st, ws.HbT ? "tc_chain_fwd_keep" : "tc_chain_fwd");
+  k_chain_fwd<DV, RG><<<m.nseq * m.H * (DV / (16 * RG)), CHAIN_THREADS, smem, st>>>(
+      m, (const bf*)q, (const bf*)k, S_in, S_out, (bf*)o, ws, lb0, lb1);
+  return cudaGetLastError();
+}
+
 template <int DV>
 cudaError_t fwd_t(const SeqMap& m, const void* q, const void* k, const void* v, const void* g,
                   const void* beta, const float* S_in, void* o, float* S_out, const TcWs& ws,
-                  cudaStream_t st) {
-  using bf = __nv_bfloat16;
+                  const FwdSplit& sp, cudaStream_t st) {
   cudaError_t e;
-  if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, st))) return e;
-  constexpr size_t smem = sizeof(FwdSmem<CHAIN_FWD, 1>);
-  if ((e = set_smem(k_chain_fwd<DV>, smem))) return e;
-  prof_mark(st, ws.HbT ? "tc_chain_fwd_keep" : "tc_chain_fwd");
-  k_chain_fwd<DV><<<m.nseq * m.H * (DV / 16), CHAIN_THREADS, smem, st>>>(
-      m, (const bf*)q, (const bf*)k, S_in, S_out, (bf*)o, ws);
+  if (sp.nseg <= 1) {
+    if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, 0, 0, st, true))) return e;
+    e = sp.chain_rg == 2 ? launch_chain_fwd<DV, 2>(m, q, k, S_in, o, S_out, ws, 0, 1 << 30, st, true)
+                         : launch_chain_fwd<DV, 1>(m, q, k, S_in, o, S_out, ws, 0, 1 << 30, st, true);
+    prof_mark(st, nullptr);
+    return e;
+  }
+  // State-transition / dense-kernel overlap: Pre of segment i + 1 on a
+  // low-priority stream while the chain carries segment i on a high-priority
+  // one; the chain's fp32 state passes between segments through the
+  // workspace exactly, so the results equal the unsplit call's bit for bit.
+  SideStreams* ss = side_streams();
+  if (!ss) return cudaErrorUnknown;
+  std::lock_guard<std::mutex> lock(ss->mu);
+  prof_mark(st, "tc_fwd_overlap");
+  if ((e = cudaEventRecord(ss->fork, st)) || (e = cudaStreamWaitEvent(ss->pre, ss->fork, 0)) ||
+      (e = cudaStreamWaitEvent(ss->chain, ss->fork, 0)))
+    return e;
+  for (int i = 0; i < sp.nseg; ++i) {
+    const int b0 = sp.b[i], b1 = sp.b[i + 1];
+    if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, b0, b1 - b0, ss->pre, false))) return e;
+    if ((e = cudaEventRecord(ss->seg[i], ss->pre))) return e;
+  }
+  for (int i = 0; i < sp.nseg; ++i) {
+    const float* sin = i == 0 ? S_in : ws.Sseg[(i - 1) & 1];
+    float* sout = i == sp.nseg - 1 ? S_out : ws.Sseg[i & 1];
+    if ((e = cudaStreamWaitEvent(ss->chain, ss->seg[i], 0))) return e;
+    e = sp.chain_rg == 2
+            ? launch_chain_fwd<DV, 2>(m, q, k, sin, o, sout, ws, sp.b[i], sp.b[i + 1], ss->chain, false)
+            : launch_chain_fwd<DV, 1>(m, q, k, sin, o, sout, ws, sp.b[i], sp.b[i + 1], ss->chain, false);
+    if (e) return e;
+  }
+  if ((e = cudaEventRecord(ss->join, ss->chain)) || (e = cudaStreamWaitEvent(st, ss->join, 0)))
+    return e;
   prof_mark(st, nullptr);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 template <int DV>
@@ -668,7 +751,7 @@ cudaError_t bwd_t(const SeqMap& m, const void* q, const void* k, const void* v, 
     prof_mark(st, nullptr);
     return cudaGetLastError();
   }
-  if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, st))) return e;
+  if ((e = tc_pre(m, DV, q, k, v, g, beta, ws, 0, 0, st, true))) return e;
   constexpr size_t s1 = sizeof(FwdSmem<CHAIN_RECOMPUTE, BWD_RG>);
   constexpr size_t s2 = sizeof(RevSmem<BWD_RG>);
   constexpr size_t smem = s1 > s2 ? s1 : s2;
@@ -687,9 +770,9 @@ cudaError_t bwd_t(const SeqMap& m, const void* q, const void* k, const void* v, 
 
 cudaError_t tc_fwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const float* S_in, void* o, float* S_out,
-                   const TcWs& ws, cudaStream_t st) {
-  if (dv == 128) return fwd_t<128>(m, q, k, v, g, beta, S_in, o, S_out, ws, st);
-  return fwd_t<256>(m, q, k, v, g, beta, S_in, o, S_out, ws, st);
+                   const TcWs& ws, const FwdSplit& sp, cudaStream_t st) {
+  if (dv == 128) return fwd_t<128>(m, q, k, v, g, beta, S_in, o, S_out, ws, sp, st);
+  return fwd_t<256>(m, q, k, v, g, beta, S_in, o, S_out, ws, sp, st);
 }
 
 cudaError_t tc_bwd(const SeqMap& m, int dv, const void* q, const void* k, const void* v,

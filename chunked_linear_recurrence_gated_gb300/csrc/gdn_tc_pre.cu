@@ -175,13 +175,17 @@ template <int DV>
 __global__ void __launch_bounds__(256, DV == 128 ? 2 : 1)
     k_pre_tc(SeqMap m, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
              const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
-             const __nv_bfloat16* __restrict__ beta, TcWs ws) {
+             const __nv_bfloat16* __restrict__ beta, TcWs ws, int seg_b0, int seg_nb) {
   using L = PreLayout<DV>;
   constexpr int DK = 128;
   constexpr int NT = 256;
   constexpr uint32_t TB = 8192;  // bytes between the 64-wide column tiles of K, Q, V
   BlockInfo bi;
-  const int gb = blockIdx.x, h = blockIdx.y, H = m.H, tid = threadIdx.x;
+  // the launch covers every block, or blocks [seg_b0, seg_b0 + seg_nb) of each
+  // sequence (one segment of a split fixed-length forward)
+  const int gb = seg_nb > 0 ? (int)(blockIdx.x / seg_nb) * m.nblk_fixed + seg_b0 + (int)(blockIdx.x % seg_nb)
+                            : (int)blockIdx.x;
+  const int h = blockIdx.y, H = m.H, tid = threadIdx.x;
   // Pre is the first kernel of a fixed-length call: it clears the status word,
   // which the later kernels of the call only ever set (varlen calls: the
   // block-table kernel sets it)
@@ -414,15 +418,17 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 template <int DV>
 cudaError_t launch_pre(const SeqMap& m, const void* q, const void* k, const void* v,
-                       const void* g, const void* beta, const TcWs& ws, cudaStream_t st) {
+                       const void* g, const void* beta, const TcWs& ws, int b0, int nb,
+                       cudaStream_t st, bool mark) {
   using bf = __nv_bfloat16;
   cudaError_t e;
   constexpr size_t smem = PreLayout<DV>::BYTES + 1024;  // + alignment of the base
   if ((e = set_smem(k_pre_tc<DV>, smem))) return e;
-  if (m.nblk_cap > 0) {
-    prof_mark(st, "tc_pre");
-    k_pre_tc<DV><<<dim3(m.nblk_cap, m.H), 256, smem, st>>>(
-        m, (const bf*)q, (const bf*)k, (const bf*)v, (const bf*)g, (const bf*)beta, ws);
+  const int gx = nb > 0 ? nb * m.nseq : m.nblk_cap;
+  if (gx > 0) {
+    if (mark) prof_mark(st, "tc_pre");
+    k_pre_tc<DV><<<dim3(gx, m.H), 256, smem, st>>>(m, (const bf*)q, (const bf*)k, (const bf*)v,
+                                                 (const bf*)g, (const bf*)beta, ws, b0, nb);
   }
   return cudaGetLastError();
 }
@@ -430,9 +436,10 @@ cudaError_t launch_pre(const SeqMap& m, const void* q, const void* k, const void
 }  // namespace
 
 cudaError_t tc_pre(const SeqMap& m, int dv, const void* q, const void* k, const void* v,
-                   const void* g, const void* beta, const TcWs& ws, cudaStream_t st) {
-  if (dv == 128) return launch_pre<128>(m, q, k, v, g, beta, ws, st);
-  return launch_pre<256>(m, q, k, v, g, beta, ws, st);
+                   const void* g, const void* beta, const TcWs& ws, int b0, int nb,
+                   cudaStream_t st, bool mark) {
+  if (dv == 128) return launch_pre<128>(m, q, k, v, g, beta, ws, b0, nb, st, mark);
+  return launch_pre<256>(m, q, k, v, g, beta, ws, b0, nb, st, mark);
 }
 
 }  // namespace gdn

@@ -95,6 +95,8 @@ def load(build_if_missing: bool = False):
     lib.gdn_noalloc_status.restype = I
     lib.gdn_diag_wait_timeout_noalloc.argtypes = [I, P]
     lib.gdn_diag_wait_timeout_noalloc.restype = I
+    lib.gdn_diag_set_fwd_split.argtypes = [I, I, I]
+    lib.gdn_diag_set_fwd_split.restype = None
     lib.gdn_chunk_saved_bytes.argtypes = [SP]
     lib.gdn_chunk_saved_bytes.restype = Z
     lib.gdn_chunk_fwd_save.argtypes = [SP] + [P] * 8 + [P, Z, P, Z, P]
@@ -370,6 +372,12 @@ def diag_wait_timeout_noalloc(limit_log2=20, stream=None) -> int:
     """The bounded-wait self-check on the no-allocation forward's scratch;
     read the outcome with gdn_noalloc_status."""
     return load().gdn_diag_wait_timeout_noalloc(limit_log2, _stream(stream))
+
+
+def set_fwd_split(segments=0, first_permille=0, chain_rg=0):
+    """Measurement override of the split forward (include/gdn_profile.h):
+    segments 1 = no split, 0 = the library's default."""
+    load().gdn_diag_set_fwd_split(segments, first_permille, chain_rg)
 
 
 def gdn_status_str(code: int) -> str:

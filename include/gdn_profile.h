@@ -38,6 +38,17 @@ const char* gdn_profile_name(int i);
  * Returns GDN_ERR_WORKSPACE / GDN_ERR_CUDA on a bad pointer / failed launch. */
 int gdn_diag_wait_timeout(void* workspace, int limit_log2, void* stream);
 
+/* Measurement override of how gdn_chunk_fwd / gdn_chunk_fwd_save carry out a
+ * fixed-length bf16 call: split the chunk into `segments` segments at 64-token
+ * block boundaries (1 = no split, 0 = the library's default) and overlap the
+ * Pre kernel of each segment with the state-transition chain of the previous
+ * one (the StateFlow review's split-and-overlap of the state transition with
+ * the dense kernels, split fraction f); with two segments the first covers
+ * first_permille / 1000 of the blocks (0 = half). chain_rg = 16-value-column
+ * groups per chain CTA (1 or 2; 0 = default). Results are bit-identical for
+ * every setting. Process-global and not thread-safe, like the timing hook. */
+void gdn_diag_set_fwd_split(int segments, int first_permille, int chain_rg);
+
 /* The same self-check on the status word of gdn_chunk_fwd_noalloc's scratch
  * on the current device; read the outcome with gdn_noalloc_status. */
 int gdn_diag_wait_timeout_noalloc(int limit_log2, void* stream);
