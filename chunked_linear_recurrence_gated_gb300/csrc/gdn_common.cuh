@@ -88,14 +88,20 @@ struct SimtWs {
 // padded shared-memory tiles with a single bulk copy.
 constexpr int TC_LDK = 136;   // padded row of 128-wide bf16 tiles
 constexpr int TC_LD64 = 72;   // padded row of 64-wide bf16 tiles
-constexpr int TC_LDU = 24;    // padded row of a 16-column U tile
+constexpr int TC_LDU = 16;    // row of a 16-column U tile (two 16-byte chunks)
+// Element (t, c) of a 16-column tile: the two 16-byte chunks of row t swap
+// places when bit 2 of t is set, so 8 consecutive rows read at one chunk hit
+// 8 different bank groups without padding.
+__host__ __device__ constexpr int u_tile_off(int t, int c) {
+  return t * TC_LDU + (((c >> 3) ^ ((t >> 2) & 1)) << 3) + (c & 7);
+}
 constexpr int TC_DEC_ROWS = 4;  // per-block vectors in TcWs::dec
 struct TcWs {
   int* status;
   float* dec;            // [nblk, H, 4, BT]   Gamma_r, e^{gamma_C - gamma_r}, gamma_r, beta_r
                          //                    (beta_r = 0 past the end of the block)
   __nv_bfloat16* W;      // [nblk, H, BT, TC_LDK]          W = T diag(beta Gamma) K
-  __nv_bfloat16* U;      // [nblk, H, dv/16, BT, TC_LDU]   U = T diag(beta) V, tile-major
+  __nv_bfloat16* U;      // [nblk, H, dv/16, BT, TC_LDU]   U = T diag(beta) V, tile-major (u_tile_off)
   __nv_bfloat16* QKM;    // [nblk, H, BT, TC_LD64]         Q K^T * Mask (j <= r)
   __nv_bfloat16* Kp;     // [nblk, H, BT, TC_LDK]          K~ = e^{gamma_C - gamma} K (padded, zero past the end)
   __nv_bfloat16* Qp;     // [nblk, H, BT, TC_LDK]          Q~ = e^{gamma} Q (padded, zero past the end)

@@ -258,8 +258,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
         uint32_t uf[4];
         {
           const int mi = l >> 3;
-          ldsm_x4_t(smem_u32(S.U + g * BT * LDU + (16 * w + 8 * (mi >> 1) + (l & 7)) * LDU +
-                             8 * (mi & 1)),
+          ldsm_x4_t(smem_u32(S.U + g * BT * LDU + u_tile_off(16 * w + 8 * (mi >> 1) + (l & 7), 8 * (mi & 1))),
                     uf[0], uf[1], uf[2], uf[3]);
         }
 #pragma unroll

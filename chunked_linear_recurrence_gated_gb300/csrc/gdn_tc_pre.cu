@@ -33,31 +33,32 @@ constexpr int LDU = TC_LDU;
 
 // ------------------------------------------------------------------ Pre
 // Shared memory (byte offsets from a 1024-aligned base). The swizzled K, Q
-// and V tiles hold rows t with 64-wide column tiles 8192 bytes apart. Once
-// the MMAs have read them, W [t][k] is staged in A's space and the
-// tile-major U at the start.
+// and V tiles hold rows t with 64-wide column tiles 8192 bytes apart. The
+// fp32 A of the inverse is dead once T is formed: T diag(beta Gamma) and
+// T diag(beta) (swizzled [t][j] tiles, the MMAs' B operands) take its space,
+// and once the MMAs have read them W [t][k] is staged there; the tile-major U
+// is staged at the start, over the input tiles.
 template <int DV>
 struct PreLayout {
   static constexpr uint32_t K = 0;                 // K (swizzled)
   static constexpr uint32_t Q = 16384;             // Q (swizzled)
   static constexpr uint32_t V = 32768;             // V (swizzled), DV / 64 tiles
-  static constexpr uint32_t A = V + DV * 128;      // fp32 A [64][68]; then W [64][LDK]
+  static constexpr uint32_t A = V + DV * 128;      // fp32 A [64][68]; then TW, TU; then W [64][LDK]
+  static constexpr uint32_t TW = A;                // T diag(beta Gamma) [64][64] (swizzled)
+  static constexpr uint32_t TU = A + 8192;         // T diag(beta) [64][64] (swizzled)
   static constexpr uint32_t TF = A + 17408;        // fp32 T [64][68]
   static constexpr uint32_t S = TF + 17408;        // fp32 [16][52] block-row product
-  static constexpr uint32_t TW = S + 4096;         // T diag(beta Gamma) [64][64] (swizzled)
-  static constexpr uint32_t TU = TW + 8192;        // T diag(beta) [64][64] (swizzled)
-  static constexpr uint32_t UST = 0;               // U, tile-major [DV/16][64][LDU]
-  static constexpr uint32_t VEC = TU + 8192;
+  static constexpr uint32_t UST = 0;               // U, tile-major [DV/16][64][LDU] (u_tile_off)
+  static constexpr uint32_t VEC = S + 4096;
   static constexpr uint32_t BYTES = VEC + 4 * 256 + 64;
   static constexpr uint32_t NCOL = 256;            // TMEM columns: W^T [0, 64), U^T [64, 64 + DV/2)
 };
-static_assert(PreLayout<128>::A % 1024 == 0 && PreLayout<128>::TW % 1024 == 0 &&
-                  PreLayout<128>::TU % 1024 == 0 && PreLayout<256>::A % 1024 == 0 &&
-                  PreLayout<256>::TW % 1024 == 0 && PreLayout<256>::TU % 1024 == 0,
+static_assert(PreLayout<128>::A % 1024 == 0 && PreLayout<256>::A % 1024 == 0,
               "swizzled tiles start 1024-byte aligned");
 static_assert(PreLayout<128>::A >= (128 / 16) * BT * TC_LDU * 2 &&
                   PreLayout<256>::A >= (256 / 16) * BT * TC_LDU * 2,
               "the tile-major U fits below A");
+static_assert(PreLayout<256>::BYTES + 1024 <= 113 * 1024, "two CTAs per SM");
 
 // Fragment loads of mma.m16n8k16 from a swizzled tile (64-wide column tiles
 // `tb` bytes apart): A rows [r0, r0+16) x cols [c0, c0+16); B for two n8
@@ -172,7 +173,7 @@ __device__ void invert_unit_lower64(const float* A, float* Tf, float* S) {
 // tensor-memory read-back warp w owns lanes [32 (w & 3), +32) and the
 // (w >> 2)-th half of the columns.
 template <int DV>
-__global__ void __launch_bounds__(256, DV == 128 ? 2 : 1)
+__global__ void __launch_bounds__(256, 2)
     k_pre_tc(SeqMap m, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
              const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
              const __nv_bfloat16* __restrict__ beta, TcWs ws, int seg_b0, int seg_nb) {
@@ -375,16 +376,15 @@ __global__ void __launch_bounds__(256, DV == 128 ? 2 : 1)
         for (int i = 0; i < 32; ++i) Wst[(32 * ch + i) * LDK + kk] = __float2bfloat16_rn(vv[i]);
       } else {
         const int vv_ = 128 * (part - 1) + 32 * lq + l;
-        __nv_bfloat16* col = Ust + (size_t)(vv_ >> 4) * BT * LDU + (vv_ & 15);
+        __nv_bfloat16* tile = Ust + (size_t)(vv_ >> 4) * BT * LDU;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) col[(32 * ch + i) * LDU] = __float2bfloat16_rn(vv[i]);
+        for (int i = 0; i < 32; ++i)
+          tile[u_tile_off(32 * ch + i, vv_ & 15)] = __float2bfloat16_rn(vv[i]);
       }
     }
-    // zero pad columns of the staged tiles
+    // zero pad columns of the staged W tile
     for (int r = tid; r < BT; r += NT)
       *reinterpret_cast<uint4*>(Wst + r * LDK + DK) = make_uint4(0u, 0u, 0u, 0u);
-    for (int r = tid; r < (DV / 16) * BT; r += NT)
-      *reinterpret_cast<uint4*>(Ust + r * LDU + 16) = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_proxy_async_smem();
   tc_fence_before();

@@ -172,9 +172,9 @@ gdn_status gdn_varlen_bwd(const gdn_shape* shape, const int* cu_seqlens, int nse
  * that loads the library until the process exits; a shape whose forward
  * workspace (gdn_chunk_workspace_bytes(shape, 0)) exceeds it is rejected with
  * GDN_ERR_WORKSPACE before anything is launched (for dk = dv = 128 bf16 the
- * forward workspace is 85 KiB per 64-token block and head plus 128 KiB per
- * sequence and head, so the limit is B * ceil(T / 64) * H <= 769 for B = H = 1
- * and <= 736 for B = 1, H = 16). The call
+ * forward workspace is 77 KiB per 64-token block and head plus 128 KiB per
+ * sequence and head, so the limit is B * ceil(T / 64) * H <= 849 for B = H = 1
+ * and <= 816 for B = 1, H = 16). The call
  * allocates nothing. Its first call on a device looks up the array's device
  * address on the current device; make that first call before any stream
  * capture. Every call on a device shares the one array and no part of it needs

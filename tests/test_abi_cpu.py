@@ -182,10 +182,10 @@ def test_conv_host_checks(lib):
 
 def test_noalloc_limit_matches_its_documentation(lib):
     """The no-allocation forward accepts exactly the shapes whose forward
-    workspace fits GDN_NOALLOC_SCRATCH_BYTES (documented as 769 block-heads
-    for one sequence and head, 736 for 16 heads, at dk = dv = 128 bf16)."""
+    workspace fits GDN_NOALLOC_SCRATCH_BYTES (documented as 849 block-heads
+    for one sequence and head, 816 for 16 heads, at dk = dv = 128 bf16)."""
     lim = 64 << 20
     fits = lambda nb, H: lib.gdn_chunk_workspace_bytes(
         ctypes.byref(shape(B=1, T=64 * nb, H=H)), 0) <= lim
-    assert fits(769, 1) and not fits(770, 1)
-    assert fits(736 // 16, 16) and not fits(736 // 16 + 1, 16)
+    assert fits(849, 1) and not fits(850, 1)
+    assert fits(816 // 16, 16) and not fits(816 // 16 + 1, 16)
