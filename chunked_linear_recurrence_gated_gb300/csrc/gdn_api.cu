@@ -313,6 +313,7 @@ SeqMap make_map(const Plan& p, const int* cu, const int* blk0, const int* blk_se
   m.nblk_fixed = p.varlen ? 0 : (p.T + BT - 1) / BT;
   m.nblk_cap = p.nblk_cap;
   m.H = p.H;
+  m.T_total = (long long)p.B * p.T;
   return m;
 }
 

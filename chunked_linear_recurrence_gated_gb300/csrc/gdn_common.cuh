@@ -27,6 +27,7 @@ struct SeqMap {
   int nblk_fixed;      // fixed: blocks per sequence
   int nblk_cap;        // global blocks launched by the per-block kernels
   int H;
+  long long T_total;   // tokens of the call (B * T, or the packed total)
 };
 
 struct BlockInfo {

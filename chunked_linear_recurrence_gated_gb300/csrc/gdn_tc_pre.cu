@@ -20,6 +20,10 @@
 // tcgen05 MMA: one thread issues them from 128-byte-swizzled shared-memory
 // tiles into tensor memory, the warps read the rows back into shared-memory
 // tiles in the chains' layouts, and bulk copies store the tiles.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "gdn_internal.cuh"
 #include "gdn_mma.cuh"
 #include "gdn_umma.cuh"
@@ -176,7 +180,9 @@ template <int DV>
 __global__ void __launch_bounds__(256, 2)
     k_pre_tc(SeqMap m, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
              const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
-             const __nv_bfloat16* __restrict__ beta, TcWs ws, int seg_b0, int seg_nb) {
+             const __nv_bfloat16* __restrict__ beta, TcWs ws, int seg_b0, int seg_nb,
+             const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             const __grid_constant__ CUtensorMap tm_v) {
   using L = PreLayout<DV>;
   constexpr int DK = 128;
   constexpr int NT = 256;
@@ -205,25 +211,30 @@ __global__ void __launch_bounds__(256, 2)
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sb + L::VEC + 4 * 256);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sb + L::VEC + 4 * 256 + 8);
   volatile int* abort = reinterpret_cast<volatile int*>(sb + L::VEC + 4 * 256 + 16);
+  uint64_t* tbar = reinterpret_cast<uint64_t*>(sb + L::VEC + 4 * 256 + 24);
   const int w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
   const int rw = w & 3, cw = w >> 2, R0 = 16 * rw;
   const int lq = w & 3, ch = w >> 2;  // TMEM lane quarter, column half
   const size_t bh = (size_t)gb * H + h;
 
-  for (int idx = tid; idx < BT * (DK / 8); idx += NT) {
-    const int r = idx >> 4, c = (idx & 15) * 8;
-    const bool ok = r < bi.len;
-    const size_t off = ((size_t)(bi.tok0 + (ok ? r : 0)) * H + h) * DK + c;
-    cp16(sb + L::K + sw128(r, c, TB), k + off, ok);
-    cp16(sb + L::Q + sw128(r, c, TB), q + off, ok);
+  // K, Q, V by tensor copies (the maps view q, k, v as [B][T][H][d] with
+  // 64 x 64 boxes and the 128-byte swizzle the tiles use), one thread issuing
+  if (tid == 0) {
+    mbar_init(tbar, 1);
+    mbar_init(mbar, 1);
+    *abort = 0;
+    fence_mbar_init();
+    mbar_arrive_expect_tx(tbar, 2 * 2 * TB + (DV / 64) * TB);
+    const int tc = m.cu ? bi.tok0 : bi.lb * BT;  // token coordinate within the sequence
+    const int sc = m.cu ? 0 : bi.seq;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      tma_load_4d(sb + L::K + hh * TB, &tm_k, 64 * hh, h, tc, sc, tbar);
+      tma_load_4d(sb + L::Q + hh * TB, &tm_q, 64 * hh, h, tc, sc, tbar);
+    }
+#pragma unroll
+    for (int vt = 0; vt < DV / 64; ++vt) tma_load_4d(sb + L::V + vt * TB, &tm_v, 64 * vt, h, tc, sc, tbar);
   }
-  for (int idx = tid; idx < BT * (DV / 8); idx += NT) {
-    const int r = idx / (DV / 8), c = (idx % (DV / 8)) * 8;
-    const bool ok = r < bi.len;
-    cp16(sb + L::V + (uint32_t)(c >> 6) * TB + sw128(r, c & 63, TB),
-         v + ((size_t)(bi.tok0 + (ok ? r : 0)) * H + h) * DV + c, ok);
-  }
-  cp_commit();
   if (tid < BT) {
     const bool ok = tid < bi.len;
     const size_t off = (size_t)(bi.tok0 + tid) * H + h;
@@ -231,17 +242,27 @@ __global__ void __launch_bounds__(256, 2)
     s_b[tid] = ok ? __bfloat162float(beta[off]) : 0.f;
   }
   if (w == 0) tmem_alloc(tslot, L::NCOL);
-  if (tid == 0) {
-    mbar_init(mbar, 1);
-    *abort = 0;
-    fence_mbar_init();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
   block_cumsum64(s_g);
-  cp_wait<0>();
+  bool ok = __all_sync(0xffffffffu, mbar_wait(tbar, 0, abort));
+  // rows past the block's end: zeros (a tail of a sequence; the tensor copy
+  // zero-fills only past the end of the tensor)
+  if (bi.len < BT) {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const int nr = BT - bi.len;
+    for (int idx = tid; idx < nr * 16; idx += NT) {
+      const int r = bi.len + (idx >> 4), c = (idx & 15) * 8;
+      *reinterpret_cast<uint4*>(sb + L::K + sw128(r, c, TB)) = z;
+      *reinterpret_cast<uint4*>(sb + L::Q + sw128(r, c, TB)) = z;
+    }
+    for (int idx = tid; idx < nr * (DV / 8); idx += NT) {
+      const int r = bi.len + idx / (DV / 8), c = (idx % (DV / 8)) * 8;
+      *reinterpret_cast<uint4*>(sb + L::V + (uint32_t)(c >> 6) * TB + sw128(r, c & 63, TB)) = z;
+    }
+  }
   __syncthreads();
   if (tid < BT) {
     const float gr = s_g[tid];
@@ -357,7 +378,7 @@ __global__ void __launch_bounds__(256, 2)
     }
     umma_commit(mbar);
   }
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(mbar, 0, abort));  // warp-uniform for tcgen05.ld
+  ok = __all_sync(0xffffffffu, mbar_wait(mbar, 0, abort)) && ok;  // warp-uniform for tcgen05.ld
   tc_fence_after();
   // read back: lane = key k (W^T) or value v (U^T), 32 tokens per warp; staged as
   // W [t][k] (padded rows) in A's space and U tile-major at the start
@@ -416,6 +437,44 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  });
+  return fn;
+}
+
+// View of a [B][T][H][d] bf16 tensor (varlen: [1][total][H][d]) as a 4-D map
+// with 64-element x 1 head x 64-token boxes and the 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* map, const void* base, int d, const SeqMap& m) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const bool varlen = m.cu != nullptr;
+  const cuuint64_t T = varlen ? (cuuint64_t)m.T_total : (cuuint64_t)m.T_fixed;
+  const cuuint64_t Bn = varlen ? 1 : (cuuint64_t)m.nseq;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)m.H, T, Bn};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)m.H * d * 2,
+                                 (cuuint64_t)m.H * d * 2 * T};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)BT, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int DV>
 cudaError_t launch_pre(const SeqMap& m, const void* q, const void* k, const void* v,
                        const void* g, const void* beta, const TcWs& ws, int b0, int nb,
@@ -426,9 +485,14 @@ cudaError_t launch_pre(const SeqMap& m, const void* q, const void* k, const void
   if ((e = set_smem(k_pre_tc<DV>, smem))) return e;
   const int gx = nb > 0 ? nb * m.nseq : m.nblk_cap;
   if (gx > 0) {
+    alignas(64) CUtensorMap tq, tk, tv;
+    if ((e = make_map(&tq, q, 128, m)) || (e = make_map(&tk, k, 128, m)) ||
+        (e = make_map(&tv, v, DV, m)))
+      return e;
     if (mark) prof_mark(st, "tc_pre");
     k_pre_tc<DV><<<dim3(gx, m.H), 256, smem, st>>>(m, (const bf*)q, (const bf*)k, (const bf*)v,
-                                                 (const bf*)g, (const bf*)beta, ws, b0, nb);
+                                                 (const bf*)g, (const bf*)beta, ws, b0, nb, tq, tk,
+                                                 tv);
   }
   return cudaGetLastError();
 }

@@ -109,3 +109,18 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 }  // namespace gdn
+
+namespace gdn {
+// 4-D tiled tensor copy global -> shared (TMA), completing its bytes on `bar`.
+// `tmap` is the address of a __grid_constant__ CUtensorMap kernel parameter;
+// c0 is the innermost coordinate (its byte offset must be a multiple of 16).
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2,
+                                            int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+}  // namespace gdn
