@@ -36,18 +36,19 @@ constexpr int LD64 = TC_LD64;
 constexpr int LDU = TC_LDU;
 
 // ------------------------------------------------------------------ Pre
-// Shared memory (byte offsets from a 1024-aligned base). The swizzled K, Q
-// and V tiles hold rows t with 64-wide column tiles 8192 bytes apart. The
-// fp32 A of the inverse is dead once T is formed: T diag(beta Gamma) and
-// T diag(beta) (swizzled [t][j] tiles, the MMAs' B operands) take its space,
-// and once the MMAs have read them W [t][k] is staged there; the tile-major U
-// is staged at the start, over the input tiles.
+// Shared memory (byte offsets from a 1024-aligned base). The swizzled K, V
+// and Q tiles hold rows t with 64-wide column tiles 8192 bytes apart. Q is
+// dead once Q K^T is formed: the fp32 A of the inverse takes its space (and
+// 1 KB past it), then T diag(beta Gamma) and T diag(beta) (swizzled [t][j]
+// tiles, the MMAs' B operands), and once the MMAs have read those, W [t][k]
+// is staged there; the tile-major U is staged over K and V. At dv = 128 this
+// is 72 KB, three CTAs per SM.
 template <int DV>
 struct PreLayout {
   static constexpr uint32_t K = 0;                 // K (swizzled)
-  static constexpr uint32_t Q = 16384;             // Q (swizzled)
-  static constexpr uint32_t V = 32768;             // V (swizzled), DV / 64 tiles
-  static constexpr uint32_t A = V + DV * 128;      // fp32 A [64][68]; then TW, TU; then W [64][LDK]
+  static constexpr uint32_t V = 16384;             // V (swizzled), DV / 64 tiles
+  static constexpr uint32_t Q = V + DV * 128;      // Q (swizzled)
+  static constexpr uint32_t A = Q;                 // fp32 A [64][68]; then TW, TU; then W [64][LDK]
   static constexpr uint32_t TW = A;                // T diag(beta Gamma) [64][64] (swizzled)
   static constexpr uint32_t TU = A + 8192;         // T diag(beta) [64][64] (swizzled)
   static constexpr uint32_t TF = A + 17408;        // fp32 T [64][68]
@@ -55,14 +56,17 @@ struct PreLayout {
   static constexpr uint32_t UST = 0;               // U, tile-major [DV/16][64][LDU] (u_tile_off)
   static constexpr uint32_t VEC = S + 4096;
   static constexpr uint32_t BYTES = VEC + 4 * 256 + 64;
-  static constexpr uint32_t NCOL = 256;            // TMEM columns: W^T [0, 64), U^T [64, 64 + DV/2)
+  static constexpr uint32_t NCOL = DV == 128 ? 128 : 256;  // TMEM: W^T [0, 64), U^T [64, 64 + DV/2)
+  static constexpr int CTAS = DV == 128 ? 3 : 2;          // per SM
 };
-static_assert(PreLayout<128>::A % 1024 == 0 && PreLayout<256>::A % 1024 == 0,
+static_assert(PreLayout<128>::Q % 1024 == 0 && PreLayout<256>::Q % 1024 == 0 &&
+                  PreLayout<128>::TF % 1024 == 0 && PreLayout<256>::TF % 1024 == 0,
               "swizzled tiles start 1024-byte aligned");
-static_assert(PreLayout<128>::A >= (128 / 16) * BT * TC_LDU * 2 &&
-                  PreLayout<256>::A >= (256 / 16) * BT * TC_LDU * 2,
-              "the tile-major U fits below A");
-static_assert(PreLayout<256>::BYTES + 1024 <= 113 * 1024, "two CTAs per SM");
+static_assert(PreLayout<128>::Q >= (128 / 16) * BT * TC_LDU * 2 &&
+                  PreLayout<256>::Q >= (256 / 16) * BT * TC_LDU * 2,
+              "the tile-major U fits over K and V");
+static_assert((PreLayout<128>::BYTES + 1024 + 1024) * 3 <= 228 * 1024, "three CTAs per SM at dv = 128");
+static_assert((PreLayout<256>::BYTES + 1024 + 1024) * 2 <= 228 * 1024, "two CTAs per SM at dv = 256");
 
 // Fragment loads of mma.m16n8k16 from a swizzled tile (64-wide column tiles
 // `tb` bytes apart): A rows [r0, r0+16) x cols [c0, c0+16); B for two n8
@@ -177,7 +181,7 @@ __device__ void invert_unit_lower64(const float* A, float* Tf, float* S) {
 // tensor-memory read-back warp w owns lanes [32 (w & 3), +32) and the
 // (w >> 2)-th half of the columns.
 template <int DV>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
     k_pre_tc(SeqMap m, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
              const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
              const __nv_bfloat16* __restrict__ beta, TcWs ws, int seg_b0, int seg_nb,
@@ -326,6 +330,7 @@ __global__ void __launch_bounds__(256, 2)
       }
     }
     __nv_bfloat16* qkm = ws.QKM + bh * BT * LD64;
+    __syncthreads();  // every warp is done reading Q before A overwrites it
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
