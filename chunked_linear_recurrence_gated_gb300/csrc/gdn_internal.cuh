@@ -1,6 +1,8 @@
 // Internal launch interface between the C-ABI host code and the kernel files.
 #pragma once
 
+#include <cuda.h>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -36,6 +38,14 @@ cudaError_t tc_bwd(const SeqMap& m, int dv, const void* q, const void* k, const 
                    const void* g, const void* beta, const float* S_in, const void* dout,
                    const float* dS_out, void* dq, void* dk_out, void* dv_out, void* dg,
                    void* dbeta, float* dS_in, const TcWs& ws, bool run_pre, cudaStream_t st);
+
+// Tensor maps for TMA copies (gdn_tc_pre.cu), 128-byte swizzle. make_tok_map
+// views a [B][T][H][d] bf16 tensor (varlen: [1][total][H][d]) with
+// 64-element x 1 head x 64-token boxes; make_ws_map a per-block-head
+// workspace array [nbh][rows][row_stride] with 64-element x box_rows boxes.
+cudaError_t make_tok_map(CUtensorMap* map, const void* base, int d, const SeqMap& m);
+cudaError_t make_ws_map(CUtensorMap* map, const void* base, int inner, int rows, int row_stride,
+                        long long nbh, int box_rows);
 
 // Diagnostic timing hook (include/gdn_profile.h): records an event before the
 // kernel named `next` (nullptr after the last kernel of a call) when armed.

@@ -461,9 +461,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // View of a [B][T][H][d] bf16 tensor (varlen: [1][total][H][d]) as a 4-D map
 // with 64-element x 1 head x 64-token boxes and the 128-byte swizzle.
-cudaError_t make_map(CUtensorMap* map, const void* base, int d, const SeqMap& m) {
+cudaError_t make_tok_map(CUtensorMap* map, const void* base, int d, const SeqMap& m) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const bool varlen = m.cu != nullptr;
@@ -480,6 +482,26 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int d, const SeqMap& m)
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+
+// View of a per-block-head workspace array [nbh][rows][row_stride] (bf16) as a
+// 3-D map whose boxes are 64 elements x box_rows rows of one block-head, with
+// the 128-byte swizzle.
+cudaError_t make_ws_map(CUtensorMap* map, const void* base, int inner, int rows, int row_stride,
+                        long long nbh, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)nbh};
+  const cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, (cuuint64_t)row_stride * 2 * rows};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+namespace {
+
 template <int DV>
 cudaError_t launch_pre(const SeqMap& m, const void* q, const void* k, const void* v,
                        const void* g, const void* beta, const TcWs& ws, int b0, int nb,
@@ -491,8 +513,8 @@ cudaError_t launch_pre(const SeqMap& m, const void* q, const void* k, const void
   const int gx = nb > 0 ? nb * m.nseq : m.nblk_cap;
   if (gx > 0) {
     alignas(64) CUtensorMap tq, tk, tv;
-    if ((e = make_map(&tq, q, 128, m)) || (e = make_map(&tk, k, 128, m)) ||
-        (e = make_map(&tv, v, DV, m)))
+    if ((e = make_tok_map(&tq, q, 128, m)) || (e = make_tok_map(&tk, k, 128, m)) ||
+        (e = make_tok_map(&tv, v, DV, m)))
       return e;
     if (mark) prof_mark(st, "tc_pre");
     k_pre_tc<DV><<<dim3(gx, m.H), 256, smem, st>>>(m, (const bf*)q, (const bf*)k, (const bf*)v,
