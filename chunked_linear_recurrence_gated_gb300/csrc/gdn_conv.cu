@@ -6,11 +6,14 @@
 //
 // HBM-bound: every thread owns 4 channels over a run of tokens, keeps the last
 // W - 1 inputs in registers as a sliding window, and reads each input row once
-// (plus a W - 1 row halo per tile), loading LA_F / LA_B tokens ahead of their use so
-// that enough bytes are in flight. Consecutive threads take consecutive
+// (plus a W - 1 row halo per tile), with enough loads in flight to cover the
+// memory latency: the forward keeps two groups of G_F tokens outstanding, the
+// backward loads LA_B tokens ahead. Consecutive threads take consecutive
 // channel groups, so every warp load is one contiguous 256-byte (bf16) or
 // 512-byte (fp32) segment.
 #include <stdint.h>
+
+#include <algorithm>
 
 #include <type_traits>
 
@@ -20,13 +23,13 @@
 namespace gdn {
 namespace {
 
-constexpr int CONV_TT = 64;    // tokens per forward tile
-constexpr int CONV_TTB = 256;  // tokens per backward tile (one dw / db partial each)
+constexpr int CONV_TT_MIN = 64;  // shortest forward tile (the launch sizes tiles to fill the GPU once)
+constexpr int CONV_TTB = 256;  // shortest backward tile (one dw / db partial each)
 constexpr int CONV_NT = 128;   // threads per block
 
 constexpr int CV = 4;          // channels per thread
-constexpr int LA_F = 4;        // tokens loaded ahead of their use (forward)
-constexpr int LA_B = 8;        // and in the backward's interior
+constexpr int G_F = 8;         // tokens per load group, two groups in flight (forward)
+constexpr int LA_B = 8;        // tokens loaded ahead of their use in the backward's interior
 
 // 4 channels: 16 bytes of fp32 or 8 bytes of bf16
 __device__ __forceinline__ void ld_vec(const float* p, float* v) {
@@ -51,6 +54,25 @@ __device__ __forceinline__ void st_vec(__nv_bfloat16* p, const float* v) {
   const __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
   *reinterpret_cast<uint2*>(p) =
       make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+}
+// 4 channels as loaded (unconverted): float4 for fp32, uint2 for bf16
+template <typename T>
+using RawVec = typename std::conditional<std::is_same<T, float>::value, float4, uint2>::type;
+template <typename T>
+__device__ __forceinline__ RawVec<T> ld_raw(const T* p) {
+  return *reinterpret_cast<const RawVec<T>*>(p);
+}
+__device__ __forceinline__ void cvt_raw(const float4& a, float* v) {
+  v[0] = a.x;
+  v[1] = a.y;
+  v[2] = a.z;
+  v[3] = a.w;
+}
+__device__ __forceinline__ void cvt_raw(const uint2& a, float* v) {
+  v[0] = __uint_as_float(a.x << 16);
+  v[1] = __uint_as_float(a.x & 0xffff0000u);
+  v[2] = __uint_as_float(a.y << 16);
+  v[3] = __uint_as_float(a.y & 0xffff0000u);
 }
 __device__ __forceinline__ void zero_vec(float* v) {
 #pragma unroll
@@ -80,8 +102,10 @@ __device__ __forceinline__ void ld_ext(const T* xrow0, const T* srow0, int s, in
     zero_vec(v);
 }
 
+// One tile of tt tokens per block row; the launch picks tt (a multiple of
+// 2 G_F) so that the tiles of a call fill the GPU's resident blocks once.
 template <typename T, int W>
-__global__ void __launch_bounds__(CONV_NT) k_conv_fwd(int Tn, int C, int act, const T* __restrict__ x,
+__global__ void __launch_bounds__(CONV_NT) k_conv_fwd(int Tn, int tt, int C, int act, const T* __restrict__ x,
                                                       const float* __restrict__ w,
                                                       const float* __restrict__ b,
                                                       const T* __restrict__ s_in, T* __restrict__ y,
@@ -98,36 +122,53 @@ __global__ void __launch_bounds__(CONV_NT) k_conv_fwd(int Tn, int C, int act, co
     for (int j = 0; j < W; ++j) wr[v][j] = w[(size_t)(c0 + v) * W + j];
     br[v] = b ? b[c0 + v] : 0.f;
   }
-  const int t0 = blockIdx.x * CONV_TT, t1 = min(t0 + CONV_TT, Tn);
+  const int t0 = blockIdx.x * tt, t1 = min(t0 + tt, Tn);
   float xw[W - 1][CV];  // x[t - W + 1 .. t - 1]
 #pragma unroll
   for (int j = 0; j < W - 1; ++j) ld_ext<T, W>(xr, sr, t0 - (W - 1) + j, Tn, C, xw[j]);
   T* yr = y + (size_t)bb * Tn * C + c0;
-  for (int t = t0; t < t1; t += LA_F) {
-    float xc[LA_F][CV];
+  // two groups of G tokens in flight: the next group's loads are issued
+  // before the current group is computed
+  RawVec<T> xa[G_F], xb[G_F];  // kept as loaded; converted when used
+  const bool full = t1 - t0 == tt;
+  auto load_group = [&](RawVec<T>* xg, int t) {
 #pragma unroll
-    for (int u = 0; u < LA_F; ++u) ld_ext<T, W>(xr, sr, t + u < t1 ? t + u : Tn, Tn, C, xc[u]);
+    for (int u = 0; u < G_F; ++u)
+      if (full || t + u < t1) xg[u] = ld_raw(xr + (size_t)(t + u) * C);
+  };
+  auto compute_group = [&](const RawVec<T>* xg, int t) {
 #pragma unroll
-    for (int u = 0; u < LA_F; ++u) {
-      if (t + u < t1) {
+    for (int u = 0; u < G_F; ++u) {
+      float xc[CV];
+      if (full || t + u < t1) {
+        cvt_raw(xg[u], xc);
         float out[CV];
 #pragma unroll
         for (int v = 0; v < CV; ++v) {
           float z = br[v];
 #pragma unroll
           for (int j = 0; j < W - 1; ++j) z = fmaf(wr[v][j], xw[j][v], z);
-          z = fmaf(wr[v][W - 1], xc[u][v], z);
+          z = fmaf(wr[v][W - 1], xc[v], z);
           out[v] = act_fwd(z, act);
         }
         st_vec(yr + (size_t)(t + u) * C, out);
+      } else {
+        zero_vec(xc);
       }
 #pragma unroll
       for (int j = 0; j < W - 2; ++j)
 #pragma unroll
         for (int v = 0; v < CV; ++v) xw[j][v] = xw[j + 1][v];
 #pragma unroll
-      for (int v = 0; v < CV; ++v) xw[W - 2][v] = xc[u][v];
+      for (int v = 0; v < CV; ++v) xw[W - 2][v] = xc[v];
     }
+  };
+  load_group(xa, t0);
+  for (int t = t0; t < t1; t += 2 * G_F) {
+    if (t + G_F < t1) load_group(xb, t + G_F);
+    compute_group(xa, t);
+    if (t + 2 * G_F < t1) load_group(xa, t + 2 * G_F);
+    if (t + G_F < t1) compute_group(xb, t + G_F);
   }
   if (s_out && blockIdx.x == gridDim.x - 1) {
     // state_out[i] = x_ext[T + i]
@@ -141,12 +182,12 @@ __global__ void __launch_bounds__(CONV_NT) k_conv_fwd(int Tn, int C, int act, co
   }
 }
 
-// One tile of CONV_TTB tokens per block row: g = dy * act'(z) with z
+// One tile of ttb tokens per block row: g = dy * act'(z) with z
 // recomputed, dx (lagging W - 1 tokens behind g), this tile's dw / db partial
 // sums, and (tile 0) dstate_in; the last W - 1 positions of x_ext also
 // receive dstate_out.
 template <typename T, int W>
-__global__ void __launch_bounds__(CONV_NT) k_conv_bwd(int Tn, int C, int act, const T* __restrict__ x,
+__global__ void __launch_bounds__(CONV_NT) k_conv_bwd(int Tn, int ttb, int C, int act, const T* __restrict__ x,
                                                       const float* __restrict__ w,
                                                       const float* __restrict__ b,
                                                       const T* __restrict__ s_in,
@@ -170,7 +211,7 @@ __global__ void __launch_bounds__(CONV_NT) k_conv_bwd(int Tn, int C, int act, co
     for (int j = 0; j < W; ++j) wr[v][j] = w[(size_t)(c0 + v) * W + j];
     br[v] = b ? b[c0 + v] : 0.f;
   }
-  const int s0 = tile * CONV_TTB, s1 = min(s0 + CONV_TTB, Tn);
+  const int s0 = tile * ttb, s1 = min(s0 + ttb, Tn);
   const int e0 = tile == 0 ? -(W - 1) : s0;  // first emitted index (tile 0 also emits dstate_in)
   const int tb = e0, te = s1 + (W - 1);
   float xw[W - 1][CV], gw[W - 1][CV], pw[CV][W], pb[CV];
@@ -324,7 +365,7 @@ gdn_status plan(const gdn_conv_shape* s, ConvPlan* p) {
   p->C = s->C;
   p->W = s->W;
   p->act = s->act;
-  p->ntiles_f = s->T > 0 ? (s->T + CONV_TT - 1) / CONV_TT : 1;
+  p->ntiles_f = s->T > 0 ? (s->T + CONV_TT_MIN - 1) / CONV_TT_MIN : 1;  // at most
   p->ntiles_b = s->T > 0 ? (s->T + CONV_TTB - 1) / CONV_TTB : 1;
   const int groups = s->C / p->vec;
   p->cblocks = (groups + CONV_NT - 1) / CONV_NT;
@@ -342,9 +383,23 @@ bool al(const void* q, size_t a) { return q == nullptr || ((uintptr_t)q % a) == 
 template <typename T, int W>
 cudaError_t launch_fwd(const ConvPlan& p, const void* x, const float* w, const float* b,
                        const void* s_in, void* y, void* s_out, cudaStream_t st) {
+  // tiles per block row: as many as the GPU holds resident blocks (divided
+  // over the block rows), so the launch runs in one wave; at least CONV_TT_MIN
+  // tokens per tile. The forward has no cross-tile sums, so the tiling does
+  // not change any result.
+  int dev = 0, sms = 0, occ = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) ||
+      (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_conv_fwd<T, W>, CONV_NT, 0)))
+    return e;
+  const long long rows = (long long)p.cblocks * p.B;
+  const long long per_row = std::max<long long>(1, (long long)std::max(occ, 1) * sms / rows);
+  long long tt = (p.T + per_row - 1) / per_row;
+  tt = std::max<long long>(CONV_TT_MIN, (tt + 2 * G_F - 1) / (2 * G_F) * (2 * G_F));
+  const int ntiles = p.T > 0 ? (int)((p.T + tt - 1) / tt) : 1;
   prof_mark(st, "conv_fwd");
-  k_conv_fwd<T, W><<<dim3(p.ntiles_f, p.cblocks, p.B), CONV_NT, 0, st>>>(
-      p.T, p.C, p.act, (const T*)x, w, b, (const T*)s_in, (T*)y, (T*)s_out);
+  k_conv_fwd<T, W><<<dim3(ntiles, p.cblocks, p.B), CONV_NT, 0, st>>>(
+      p.T, (int)tt, p.C, p.act, (const T*)x, w, b, (const T*)s_in, (T*)y, (T*)s_out);
   prof_mark(st, nullptr);
   return cudaGetLastError();
 }
@@ -353,15 +408,26 @@ template <typename T, int W>
 cudaError_t launch_bwd(const ConvPlan& p, const void* x, const float* w, const float* b,
                        const void* s_in, const void* dy, const void* ds_out, void* dx, float* dw,
                        float* db, void* ds_in, float* part, cudaStream_t st) {
+  // tiles as for the forward (one wave), at least CONV_TTB tokens each, so the
+  // partial sums fit the workspace sized for CONV_TTB-token tiles
+  int dev = 0, sms = 0, occ = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) ||
+      (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_conv_bwd<T, W>, CONV_NT, 0)))
+    return e;
+  const long long rows = (long long)p.cblocks * p.B;
+  const long long per_row = std::max<long long>(1, (long long)std::max(occ, 1) * sms / rows);
+  long long tt = (p.T + per_row - 1) / per_row;
+  tt = std::max<long long>(CONV_TTB, (tt + LA_B - 1) / LA_B * LA_B);
+  const int ntiles = p.T > 0 ? (int)((p.T + tt - 1) / tt) : 1;
   prof_mark(st, "conv_bwd");
-  k_conv_bwd<T, W><<<dim3(p.ntiles_b, p.cblocks, p.B), CONV_NT, 0, st>>>(
-      p.T, p.C, p.act, (const T*)x, w, b, (const T*)s_in, (const T*)dy, (const T*)ds_out, (T*)dx,
-      (T*)ds_in, part);
-  cudaError_t e = cudaGetLastError();
-  if (e) return e;
+  k_conv_bwd<T, W><<<dim3(ntiles, p.cblocks, p.B), CONV_NT, 0, st>>>(
+      p.T, (int)tt, p.C, p.act, (const T*)x, w, b, (const T*)s_in, (const T*)dy, (const T*)ds_out,
+      (T*)dx, (T*)ds_in, part);
+  if ((e = cudaGetLastError())) return e;
   prof_mark(st, "conv_reduce");
   const int n = p.C * (p.W + 1);
-  k_conv_reduce<<<(n + 255) / 256, 256, 0, st>>>(p.B * p.ntiles_b, p.C, p.W, part, dw, db);
+  k_conv_reduce<<<(n + 255) / 256, 256, 0, st>>>(p.B * ntiles, p.C, p.W, part, dw, db);
   prof_mark(st, nullptr);
   return cudaGetLastError();
 }
