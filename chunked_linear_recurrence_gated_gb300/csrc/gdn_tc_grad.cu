@@ -294,6 +294,14 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
   };
 
+  uint32_t dkp[8];  // the previous block-head's dk (this thread's key, 16 tokens), bf16 pairs
+  // stores dkp for the block-head at (tok0_, len_, h_)
+  auto store_dk = [&](int tok0_, int len_, int h_) {
+    unsigned short* dst = reinterpret_cast<unsigned short*>(dk) + ((size_t)(tok0_ + c0) * H + h_) * 128 + lane;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (c0 + i < len_) dst[(size_t)i * H * 128] = (unsigned short)(dkp[i >> 1] >> (16 * (i & 1)));
+  };
   uint32_t phS = 0, phQ = 0, phK = 0, phT = 0, phQM = 0, phKM = 0, phD = 0, phM = 0;  // phD: bit per buffer
   BlockInfo bi;
   int it = next_valid(blockIdx.x, bi);
@@ -378,6 +386,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         umma_commit(barM);
       }
       if (epi) {
+        if (prev && p == 0) store_dk(ptok0, plen, ph);  // the previous block-head's dk
         // <dH, H_b> over this pass: the two tiles share one layout
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -657,18 +666,20 @@ __global__ void __launch_bounds__(NTHR, 1)
     tc_fence_after();
     if (ctl && more) issue_qk(nit, nbi, SL::KK, &tm.k, barK);  // K is free
 
-    // ---- dk = diag(e^{gamma_C - gamma}) Kt + (P^T Q + (BE + BE^T) K) - diag(beta Gamma) T^T HW
+    // ---- dk = diag(e^{gamma_C - gamma}) Kt + (P^T Q + (BE + BE^T) K) - diag(beta Gamma) T^T HW,
+    //      kept as bf16 pairs and stored while the next block-head's first products run
     if (epi) {
       float a[16], b[16], x[16];
       tmem_ld16(tl + TC::KT, a);
       tmem_ld16(tl + TC::DK, b);
       tmem_ld16(tl + TC::XG, x);
-      __nv_bfloat16* dst = dk + ((size_t)(tok0 + c0) * H + h) * 128 + lane;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int s = c0 + i;
-        if (s < len) dst[(size_t)i * H * 128] = __float2bfloat16_rn(sDte[s] * a[i] + b[i] - sB[s] * sG[s] * x[i]);
+        a[i] = sDte[s] * a[i] + b[i] - sB[s] * sG[s] * x[i];
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dkp[i] = pack_bf16(a[2 * i], a[2 * i + 1]);
     }
     tc_fence_before();
     prev = true;
@@ -680,6 +691,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     it = nit;
     bi = nbi;
   }
+  if (epi && prev) store_dk(ptok0, plen, ph);
   if (w == CTL_WARP) {
     if (prev)
       finish_vectors(reinterpret_cast<const float*>(sb + SL::VEC + (buf ^ 1) * SL::VEC_STRIDE), ptok0, plen, ph);
