@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     tc_fence_after();
 
     // ---- E1: q . OH and k . Kt over keys; HW^T -> smem; dv; P and the sums of OV * QKM
+    uint32_t dvp[NP][8];  // dv of this thread's value column(s), bf16 pairs
     if (epi) {
       const int key = lane;
       const uint32_t kt = (uint32_t)(key >> 6) * 8 * KB;
@@ -455,14 +456,13 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
       tmem_ld16(tl + TC::HW, x);
       st_row16(sb + SL::HWT, key, c0, x);
-      // dv = diag(beta) Y: Y^T rows are value columns
-#pragma unroll 1
+      // dv = diag(beta) Y (Y^T rows are value columns), stored once the next products run
+#pragma unroll
       for (int p = 0; p < NP; ++p) {
         tmem_ld16(tl + TC::Y + 64 * p, x);
-        __nv_bfloat16* dst = dvo + ((size_t)(tok0 + c0) * H + h) * DV + 128 * p + lane;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (c0 + i < len) dst[(size_t)i * H * DV] = __float2bfloat16_rn(sB[c0 + i] * x[i]);
+        for (int i = 0; i < 8; ++i)
+          dvp[p][i] = pack_bf16(sB[c0 + 2 * i] * x[2 * i], sB[c0 + 2 * i + 1] * x[2 * i + 1]);
       }
       float acc = 0.f;
       if (upper) {
@@ -517,6 +517,16 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
       umma_commit(barM);
     }
+    if (epi) {
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        unsigned short* dst =
+            reinterpret_cast<unsigned short*>(dvo) + ((size_t)(tok0 + c0) * H + h) * DV + 128 * p + lane;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (c0 + i < len) dst[(size_t)i * H * DV] = (unsigned short)(dvp[p][i >> 1] >> (16 * (i & 1)));
+      }
+    }
     if (tid < BT) {
       const int t = tid;
       const float qo = scr[t] + scr[64 + t] + scr[128 + t] + scr[192 + t];
@@ -539,14 +549,14 @@ __global__ void __launch_bounds__(NTHR, 1)
 
     // ---- dq = diag(Gamma) OH + P K (key rows: one key column of 16 tokens per thread)
     //      E2 (rows s, lower): dT^T = diag(beta) (WV^T - diag(Gamma) HK^T); the T^T-weighted sums
+    uint32_t dqp[8];  // dq of this thread's key, bf16 pairs; stored once Z1 runs
     if (epi) {
       float a[16], b[16];
       tmem_ld16(tl + TC::OH, a);
       tmem_ld16(tl + TC::DQ, b);
-      __nv_bfloat16* dst = dq + ((size_t)(tok0 + c0) * H + h) * 128 + lane;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (c0 + i < len) dst[(size_t)i * H * 128] = __float2bfloat16_rn(sG[c0 + i] * a[i] + b[i]);
+      for (int i = 0; i < 8; ++i)
+        dqp[i] = pack_bf16(sG[c0 + 2 * i] * a[2 * i] + b[2 * i], sG[c0 + 2 * i + 1] * a[2 * i + 1] + b[2 * i + 1]);
     }
     if (lower) {
       const int s = lane - 64;
@@ -577,6 +587,12 @@ __global__ void __launch_bounds__(NTHR, 1)
         mma(TC::Z1, mdesc(su + SL::TT + 2048 * kk, SL::DTT - SL::TT), kdesc(su + SL::DTT + 32 * kk), ID_MK,
             kk > 0);
       umma_commit(barM);
+    }
+    if (epi) {
+      unsigned short* dst = reinterpret_cast<unsigned short*>(dq) + ((size_t)(tok0 + c0) * H + h) * 128 + lane;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (c0 + i < len) dst[(size_t)i * H * 128] = (unsigned short)(dqp[i >> 1] >> (16 * (i & 1)));
     }
     if (tid >= BT && tid < 2 * BT) {
       const int s = tid - BT;
