@@ -460,7 +460,7 @@ def e2e_measure(runner, K, dev):
     return ms / K, h2d, d2h, (local[0] if local else None)
 
 
-def conv_measure(K, warmup, dev, hbm, peak_kind):
+def conv_measure(K, warmup, dev, hbm, peak_kind, tokens=0):
     """The causal short convolution carried across chunks (the auxiliary
     local-convolution states), measured on a Gated DeltaNet layer's q / k / v
     convolution of the same 256K-token sequence: fwd over the 8 chained chunks,
@@ -469,7 +469,12 @@ def conv_measure(K, warmup, dev, hbm, peak_kind):
     from chunked_linear_recurrence_gated_gb300 import gdn
     from chunked_linear_recurrence_gated_gb300.inputs import CONV_BENCH, make_conv_inputs
 
-    cfg = CONV_BENCH
+    cfg = dict(CONV_BENCH)
+    if tokens:  # the first chunks up to `tokens` (small profiling cases)
+        keep = [c for i, c in enumerate(cfg["chunks"]) if sum(cfg["chunks"][:i + 1]) <= tokens]
+        if not keep:
+            raise SystemExit("--tokens is smaller than the convolution's first chunk")
+        cfg.update(chunks=keep, T=sum(keep))
     B, T, C, W, act = cfg["B"], cfg["T"], cfg["C"], cfg["W"], cfg["act"]
     d = make_conv_inputs(B, T, C, W, dtype=torch.bfloat16, device=dev, with_state=False)
     y = torch.empty_like(d["x"])
@@ -507,7 +512,8 @@ def conv_measure(K, warmup, dev, hbm, peak_kind):
     kernels = {k: {"ms_per_step": v, "alg_gb_per_s": (kb[k] / (v / 1e3) / 1e9) if k in kb else None,
                    "frac": (kb[k] / (v / 1e3) / 1e9 / hbm) if k in kb else None}
                for k, v in per.items()}
-    return {"workload": f"qkv short conv B{B} T{T} C{C} W{W} {act} bf16, 8 x 32768 chained",
+    return {"workload": f"qkv short conv B{B} T{T} C{C} W{W} {act} bf16, "
+                        f"{n} x {max(cfg['chunks'])} chained",
             "ms_per_step": ms, "tokens_per_s": B * T / (ms / 1e3),
             "alg_bytes_per_step": alg,
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": hbm,
@@ -722,6 +728,9 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="run only the first N tokens (a whole number of chunks); "
                          "for small profiling cases")
+    ap.add_argument("--conv-only", action="store_true",
+                    help="time only the short convolution (with --tokens, its first chunks); "
+                         "prints its summary; for profiling")
     args = ap.parse_args()
 
     import dataclasses
@@ -757,6 +766,13 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
 
+    if args.conv_only:
+        hbm, _, _, peak_kind = peaks()
+        conv = conv_measure(max(3, min(args.steps, 10)), args.warmup, dev, hbm, peak_kind,
+                            tokens=args.tokens)
+        if rank == 0:
+            print(json.dumps({"short_conv": conv}))
+        return
     varlen = w.seqlens is not None
     runner = VarlenRunner(w, dev) if varlen else Runner(w, dev, reuse=not recompute)
     for _ in range(max(args.warmup, 3)):
