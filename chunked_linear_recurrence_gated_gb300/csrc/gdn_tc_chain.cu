@@ -21,10 +21,12 @@
 //   dV^new = QKM^T dO + K~ dH ;  dH <- Gamma_C dH + Q~^T dO - W^T dV^new
 // The backward call runs the recompute chain (which rebuilds H_b and V^new
 // from S_in) and the reverse chain concurrently: they depend only on Pre.
+#include <cstddef>
 #include <mutex>
 
 #include "gdn_internal.cuh"
 #include "gdn_mma.cuh"
+#include "gdn_umma.cuh"
 
 namespace gdn {
 namespace {
@@ -69,13 +71,27 @@ SideStreams* side_streams() {
   return per_dev[dev];
 }
 
+// Fragment loads of mma.m16n8k16 from a 128-byte-swizzled tile (64-wide column
+// tiles `tb` bytes apart; sw128 of gdn_umma.cuh), with the lane -> (row,
+// column) assignment of ldb_nk_x2n and ldb_kn_x2n. Q~ and QKM arrive in this
+// layout.
+__device__ __forceinline__ void ldb_nk_sw(uint32_t* b, uint32_t base, uint32_t tb, int n0, int k0) {
+  const int l = threadIdx.x & 31, mat = l >> 3;
+  ldsm_x4(base + sw128(n0 + (l & 7) + (mat >> 1) * 8, k0 + (mat & 1) * 8, tb), b[0], b[1], b[2], b[3]);
+}
+__device__ __forceinline__ void ldb_kn_sw(uint32_t* b, uint32_t base, uint32_t tb, int k0, int n0) {
+  const int l = threadIdx.x & 31, mat = l >> 3;
+  ldsm_x4_t(base + sw128(k0 + (l & 7) + (mat & 1) * 8, n0 + (mat >> 1) * 8, tb), b[0], b[1], b[2],
+            b[3]);
+}
+
 // ------------------------------------------------------------------ forward / recompute
 template <int MODE, int RG>
 struct FwdStage {
   __nv_bfloat16 W[BT * LDK];
   __nv_bfloat16 K[BT * LDK];
-  __nv_bfloat16 Q[MODE == CHAIN_FWD ? BT * LDK : 8];
-  __nv_bfloat16 QKM[MODE == CHAIN_FWD ? BT * LD64 : 8];
+  __nv_bfloat16 Q[MODE == CHAIN_FWD ? 2 * BT * 64 : 8];  // swizzled [t][64 key] tiles
+  __nv_bfloat16 QKM[MODE == CHAIN_FWD ? BT * 64 : 8];    // swizzled [t][j] tile
   __nv_bfloat16 U[RG * BT * LDU];
   float dec[3 * BT];
 };
@@ -95,6 +111,12 @@ struct FwdSmem {
   __nv_bfloat16 O[MODE == CHAIN_FWD ? BT * (16 * RG + 8) : 8];
   int abort;
 };
+using FwdStage2 = FwdStage<CHAIN_FWD, 2>;
+static_assert(sizeof(FwdStage<CHAIN_FWD, 1>) % 16 == 0 && sizeof(FwdStage2) % 16 == 0 &&
+                  sizeof(FwdStage<CHAIN_RECOMPUTE, 2>) % 16 == 0 && offsetof(FwdStage2, Q) % 16 == 0 &&
+                  offsetof(FwdStage2, QKM) % 16 == 0 && offsetof(FwdStage2, U) % 16 == 0 &&
+                  offsetof(FwdStage2, dec) % 16 == 0,
+              "chain copy destinations start on 16 bytes");
 
 // Blocks [lb0, min(lb1, nblk)) of each sequence: the whole sequence, or one
 // segment of a split forward call (the state enters from S_in and leaves
@@ -168,7 +190,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
       FwdStage<MODE, RG>& S = sm.st[st];
       const size_t bh = (size_t)(si.blk0 + lb) * H + h;
       const uint32_t bytes = 2 * BT * LDK * 2 + RG * BT * LDU * 2 + 3 * BT * 4 +
-                             (MODE == CHAIN_FWD ? BT * LDK * 2 + BT * LD64 * 2 : 0);
+                             (MODE == CHAIN_FWD ? 3 * BT * 64 * 2 : 0);
       if (l == 0) {
         uint64_t* fb = &sm.full[st];
         mbar_arrive_expect_tx(fb, bytes);
@@ -177,8 +199,8 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
         bulk_g2s(S.dec, ws.dec + bh * TC_DEC_ROWS * BT, 3 * BT * 4, fb);
         bulk_g2s(S.U, ws.U + (bh * (DV / 16) + (size_t)tile * RG) * BT * LDU, RG * BT * LDU * 2, fb);
         if (MODE == CHAIN_FWD) {
-          bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, BT * LDK * 2, fb);
-          bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, fb);
+          bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, 2 * BT * 64 * 2, fb);
+          bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * 64 * 2, fb);
         }
       }
       ++issued;
@@ -230,7 +252,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
 #pragma unroll
             for (int kc = 0; kc < DK / 16; ++kc) {
               uint32_t bQ[4];
-              ldb_nk_x2n(bQ, S.Q, LDK, 16 * w, 16 * kc);
+              ldb_nk_sw(bQ, smem_u32(S.Q), 8192, 16 * w, 16 * kc);
               mma16816(o1[g][kc & 1][0], aH[kc], bQ[0], bQ[1]);
               mma16816(o1[g][kc & 1][1], aH[kc], bQ[2], bQ[3]);
             }
@@ -285,7 +307,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
       for (int kc = 0; kc < 4; ++kc) {
         ldb_kn_x2n(&bK[kc][0], S.K, LDK, 16 * kc, 32 * w);
         ldb_kn_x2n(&bK[kc][4], S.K, LDK, 16 * kc, 32 * w + 16);
-        if (MODE == CHAIN_FWD) ldb_nk_x2n(bM[kc], S.QKM, LD64, 16 * w, 16 * kc);
+        if (MODE == CHAIN_FWD) ldb_nk_sw(bM[kc], smem_u32(S.QKM), 0, 16 * w, 16 * kc);
       }
       named_bar(1, 128);
 
@@ -386,8 +408,8 @@ template <int RG>
 struct RevStage {
   __nv_bfloat16 W[BT * LDK];
   __nv_bfloat16 K[BT * LDK];
-  __nv_bfloat16 Q[BT * LDK];
-  __nv_bfloat16 QKM[BT * LD64];
+  __nv_bfloat16 Q[2 * BT * 64];  // swizzled [t][64 key] tiles
+  __nv_bfloat16 QKM[BT * 64];    // swizzled [t][j] tile
   __nv_bfloat16 dO[BT * (16 * RG + 8)];
   float dec[3 * BT];
 };
@@ -403,6 +425,10 @@ struct RevSmem {
   __nv_bfloat16 dVT[16 * RG * LD64];  // -dV^new^T (value rows)
   int abort;
 };
+static_assert(sizeof(RevStage<1>) % 16 == 0 && sizeof(RevStage<2>) % 16 == 0 &&
+                  offsetof(RevStage<2>, Q) % 16 == 0 && offsetof(RevStage<2>, QKM) % 16 == 0 &&
+                  offsetof(RevStage<2>, dO) % 16 == 0 && offsetof(RevStage<2>, dec) % 16 == 0,
+              "reverse-chain copy destinations start on 16 bytes");
 
 template <int DV, int RG>
 __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
@@ -467,14 +493,14 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
       const int lb = si.nblk - 1 - it;
       const int tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
       const size_t bh = (size_t)(si.blk0 + lb) * H + h;
-      const uint32_t bytes = 3 * BT * LDK * 2 + BT * LD64 * 2 + 3 * BT * 4;
+      const uint32_t bytes = 2 * BT * LDK * 2 + 3 * BT * 64 * 2 + 3 * BT * 4;
       if (l == 0) {
         uint64_t* fb = &sm.full[st];
         mbar_arrive_expect_tx(fb, bytes);
         bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, fb);
         bulk_g2s(S.K, ws.Kp + bh * BT * LDK, BT * LDK * 2, fb);
-        bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, BT * LDK * 2, fb);
-        bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * LD64 * 2, fb);
+        bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, 2 * BT * 64 * 2, fb);
+        bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * 64 * 2, fb);
         bulk_g2s(S.dec, ws.dec + bh * TC_DEC_ROWS * BT, 3 * BT * 4, fb);
       }
       // the dO tile: 16-byte cp.async per lane, rows past the block's end zero-filled
@@ -514,7 +540,7 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
 #pragma unroll
         for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_x2n(bK[kc], S.K, LDK, 16 * w, 16 * kc);
 #pragma unroll
-        for (int kc = 0; kc < 4; ++kc) ldb_kn_x2n(bM[kc], S.QKM, LD64, 16 * kc, 16 * w);
+        for (int kc = 0; kc < 4; ++kc) ldb_kn_sw(bM[kc], smem_u32(S.QKM), 0, 16 * kc, 16 * w);
 #pragma unroll
         for (int g = 0; g < RG; ++g) {
           float a1[2][4], a2[2][2][4];
@@ -566,8 +592,8 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
       uint32_t bQ[4][8], bW[4][8];
 #pragma unroll
       for (int kc = 0; kc < 4; ++kc) {
-        ldb_kn_x2n(&bQ[kc][0], S.Q, LDK, 16 * kc, 32 * w);
-        ldb_kn_x2n(&bQ[kc][4], S.Q, LDK, 16 * kc, 32 * w + 16);
+        ldb_kn_sw(&bQ[kc][0], smem_u32(S.Q), 8192, 16 * kc, 32 * w);
+        ldb_kn_sw(&bQ[kc][4], smem_u32(S.Q), 8192, 16 * kc, 32 * w + 16);
         ldb_kn_x2n(&bW[kc][0], S.W, LDK, 16 * kc, 32 * w);
         ldb_kn_x2n(&bW[kc][4], S.W, LDK, 16 * kc, 32 * w + 16);
       }

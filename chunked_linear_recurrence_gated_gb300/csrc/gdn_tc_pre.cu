@@ -7,11 +7,11 @@
 //         W = T diag(beta Gamma) K, U = T diag(beta) V, QKM = Q K^T * Mask
 //   ST  : V^new = U - W H_b ; H_{b+1} = Gamma_C H_b + K^T diag(e^{gamma_C - gamma}) V^new
 //   Out : O = diag(Gamma) Q H_b + QKM V^new
-// Pre also writes padded, decay-scaled copies of the block's rows,
-// K~ = diag(e^{gamma_C - gamma}) K and Q~ = diag(e^{gamma}) Q, and the per-row
-// vectors (Gamma_r, e^{gamma_C - gamma_r}, gamma_r, beta_r), so that the
-// sequential chains fetch every operand with one bulk copy and scale nothing
-// but the state.
+// Pre also writes decay-scaled copies of the block's rows,
+// K~ = diag(e^{gamma_C - gamma}) K (padded rows) and Q~ = diag(e^{gamma}) Q
+// (128-byte-swizzled tiles, as QKM), and the per-row vectors (Gamma_r,
+// e^{gamma_C - gamma_r}, gamma_r, beta_r), so that the sequential chains fetch
+// every operand with one bulk copy and scale nothing but the state.
 //
 // K K^T and Q K^T (64 x 64, reduced over the 128 keys) are warp-level MMAs
 // and the inverse is fp32 with TF32 MMAs for its off-diagonal blocks. W and U
@@ -280,18 +280,21 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
     dec[3 * BT + tid] = s_b[tid];
   }
   __syncthreads();
-  // padded, decay-scaled copies for the chains (one bulk copy each per block):
-  // K~ = diag(e^{gamma_C - gamma}) K and Q~ = diag(e^{gamma}) Q; the pad
-  // columns are written as zeros so every sector is written in full
+  // decay-scaled copies for the chains (one bulk copy each per block):
+  // K~ = diag(e^{gamma_C - gamma}) K with padded rows (the pad columns written
+  // as zeros so every sector is written in full) and Q~ = diag(e^{gamma}) Q
+  // in the swizzled layout of the shared-memory tile (the forward chain's
+  // tensor-core operand)
   {
     uint4* gK = reinterpret_cast<uint4*>(ws.Kp + bh * BT * LDK);
-    uint4* gQ = reinterpret_cast<uint4*>(ws.Qp + bh * BT * LDK);
+    unsigned char* gQ = reinterpret_cast<unsigned char*>(ws.Qp + bh * BT * LDK);
     for (int idx = tid; idx < BT * (LDK / 8); idx += NT) {
       const int r = idx / (LDK / 8), c = (idx % (LDK / 8)) * 8;
       uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
       if (c < DK) {
-        a = *reinterpret_cast<const uint4*>(sb + L::K + sw128(r, c, TB));
-        b = *reinterpret_cast<const uint4*>(sb + L::Q + sw128(r, c, TB));
+        const uint32_t off = sw128(r, c, TB);
+        a = *reinterpret_cast<const uint4*>(sb + L::K + off);
+        b = *reinterpret_cast<const uint4*>(sb + L::Q + off);
         const float sk = s_dte[r], sq = s_G[r];
         uint32_t* pa = &a.x;
         uint32_t* pb = &b.x;
@@ -301,9 +304,9 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
           pa[e] = pack_bf16(sk * x.x, sk * x.y);
           pb[e] = pack_bf16(sq * y.x, sq * y.y);
         }
+        *reinterpret_cast<uint4*>(gQ + off) = b;
       }
       gK[idx] = a;
-      gQ[idx] = b;
     }
   }
 
@@ -347,7 +350,7 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
         sA[r * 68 + c + 1] = br * km1;
         if (ws.KKM)
           *reinterpret_cast<uint32_t*>(ws.KKM + bh * BT * LD64 + r * LD64 + c) = pack_bf16(km0, km1);
-        *reinterpret_cast<uint32_t*>(qkm + r * LD64 + c) =
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(qkm) + sw128(r, c, 0)) =
             pack_bf16(qk[j][2 * hf] * d0, qk[j][2 * hf + 1] * d1);
       }
   }
@@ -424,13 +427,11 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
       ws.status[0] = DEV_TIMEOUT;
     }
   }
-  // zero the pad columns of the other padded tiles
-  {
+  // zero the pad columns of K K^T * Mask
+  if (ws.KKM) {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    for (int r = tid; r < BT; r += NT) {
-      *reinterpret_cast<uint4*>(ws.QKM + bh * BT * LD64 + r * LD64 + BT) = z;
-      if (ws.KKM) *reinterpret_cast<uint4*>(ws.KKM + bh * BT * LD64 + r * LD64 + BT) = z;
-    }
+    for (int r = tid; r < BT; r += NT)
+      *reinterpret_cast<uint4*>(ws.KKM + bh * BT * LD64 + r * LD64 + BT) = z;
   }
   if (tid == 0) bulk_wait_read();  // the staged tiles stay valid until read
   __syncthreads();
