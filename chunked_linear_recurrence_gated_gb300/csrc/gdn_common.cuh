@@ -101,17 +101,19 @@ struct TcWs {
   int* status;
   float* dec;            // [nblk, H, 4, BT]   Gamma_r, e^{gamma_C - gamma_r}, gamma_r, beta_r
                          //                    (beta_r = 0 past the end of the block)
-  __nv_bfloat16* W;      // [nblk, H, BT, TC_LDK]          W = T diag(beta Gamma) K
+  __nv_bfloat16* W;      // [nblk, H, BT, TC_LDK]          W = T diag(beta Gamma) K: the first 2 x BT x 64
+                         //                    elements of each block-head hold two 128-byte-swizzled
+                         //                    [t][64 key] tiles (sw128 of gdn_umma.cuh)
   __nv_bfloat16* U;      // [nblk, H, dv/16, BT, TC_LDU]   U = T diag(beta) V, tile-major (u_tile_off)
   __nv_bfloat16* QKM;    // [nblk, H, BT, TC_LD64]         Q K^T * Mask (j <= r): the first BT x 64
                          //                    elements of each block-head hold one 128-byte-swizzled
                          //                    [t][j] tile (sw128 of gdn_umma.cuh)
-  __nv_bfloat16* Kp;     // [nblk, H, BT, TC_LDK]          K~ = e^{gamma_C - gamma} K (padded, zero past the end)
+  __nv_bfloat16* Kp;     // [nblk, H, BT, TC_LDK]          K~ = e^{gamma_C - gamma} K, as W (zero past the end)
   __nv_bfloat16* Qp;     // [nblk, H, BT, TC_LDK]          Q~ = e^{gamma} Q: the first 2 x BT x 64 elements
                          //                    of each block-head hold two 128-byte-swizzled [t][64 key]
                          //                    tiles (keys 0-63, 64-127; zero past the end)
   __nv_bfloat16* T;      // [nblk, H, BT, BT]      (I + A)^-1          (backward)
-  __nv_bfloat16* KKM;    // [nblk, H, BT, TC_LD64] K K^T * Mask, strictly lower (backward)
+  __nv_bfloat16* KKM;    // [nblk, H, BT, TC_LD64] K K^T * Mask, strictly lower, as QKM (backward)
   __nv_bfloat16* HbT;    // [nblk, H, dv, 128]     H_b^T               (backward)
   __nv_bfloat16* VnT;    // [nblk, H, dv, BT]      V^new^T             (backward)
   __nv_bfloat16* dHT;    // [nblk, H, dv, 128]     dH_{b+1}^T          (backward)

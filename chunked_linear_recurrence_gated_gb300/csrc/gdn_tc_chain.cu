@@ -88,8 +88,8 @@ __device__ __forceinline__ void ldb_kn_sw(uint32_t* b, uint32_t base, uint32_t t
 // ------------------------------------------------------------------ forward / recompute
 template <int MODE, int RG>
 struct FwdStage {
-  __nv_bfloat16 W[BT * LDK];
-  __nv_bfloat16 K[BT * LDK];
+  __nv_bfloat16 W[2 * BT * 64];  // swizzled [t][64 key] tiles
+  __nv_bfloat16 K[2 * BT * 64];  // swizzled [t][64 key] tiles
   __nv_bfloat16 Q[MODE == CHAIN_FWD ? 2 * BT * 64 : 8];  // swizzled [t][64 key] tiles
   __nv_bfloat16 QKM[MODE == CHAIN_FWD ? BT * 64 : 8];    // swizzled [t][j] tile
   __nv_bfloat16 U[RG * BT * LDU];
@@ -189,13 +189,13 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
       if (i >= NS && !mbar_wait(&sm.empty[st], (kf - 1) & 1, abort)) break;
       FwdStage<MODE, RG>& S = sm.st[st];
       const size_t bh = (size_t)(si.blk0 + lb) * H + h;
-      const uint32_t bytes = 2 * BT * LDK * 2 + RG * BT * LDU * 2 + 3 * BT * 4 +
+      const uint32_t bytes = 4 * BT * 64 * 2 + RG * BT * LDU * 2 + 3 * BT * 4 +
                              (MODE == CHAIN_FWD ? 3 * BT * 64 * 2 : 0);
       if (l == 0) {
         uint64_t* fb = &sm.full[st];
         mbar_arrive_expect_tx(fb, bytes);
-        bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, fb);
-        bulk_g2s(S.K, ws.Kp + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.W, ws.W + bh * BT * LDK, 2 * BT * 64 * 2, fb);
+        bulk_g2s(S.K, ws.Kp + bh * BT * LDK, 2 * BT * 64 * 2, fb);
         bulk_g2s(S.dec, ws.dec + bh * TC_DEC_ROWS * BT, 3 * BT * 4, fb);
         bulk_g2s(S.U, ws.U + (bh * (DV / 16) + (size_t)tile * RG) * BT * LDU, RG * BT * LDU * 2, fb);
         if (MODE == CHAIN_FWD) {
@@ -237,7 +237,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
       {
         uint32_t bW[DK / 16][4];
 #pragma unroll
-        for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_x2n(bW[kc], S.W, LDK, 16 * w, 16 * kc);
+        for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_sw(bW[kc], smem_u32(S.W), 8192, 16 * w, 16 * kc);
 #pragma unroll
         for (int g = 0; g < RG; ++g) {
           uint32_t aH[DK / 16][4];
@@ -305,8 +305,8 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
       uint32_t bK[4][8], bM[4][4];
 #pragma unroll
       for (int kc = 0; kc < 4; ++kc) {
-        ldb_kn_x2n(&bK[kc][0], S.K, LDK, 16 * kc, 32 * w);
-        ldb_kn_x2n(&bK[kc][4], S.K, LDK, 16 * kc, 32 * w + 16);
+        ldb_kn_sw(&bK[kc][0], smem_u32(S.K), 8192, 16 * kc, 32 * w);
+        ldb_kn_sw(&bK[kc][4], smem_u32(S.K), 8192, 16 * kc, 32 * w + 16);
         if (MODE == CHAIN_FWD) ldb_nk_sw(bM[kc], smem_u32(S.QKM), 0, 16 * w, 16 * kc);
       }
       named_bar(1, 128);
@@ -406,8 +406,8 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
 // ------------------------------------------------------------------ reverse chain
 template <int RG>
 struct RevStage {
-  __nv_bfloat16 W[BT * LDK];
-  __nv_bfloat16 K[BT * LDK];
+  __nv_bfloat16 W[2 * BT * 64];  // swizzled [t][64 key] tiles
+  __nv_bfloat16 K[2 * BT * 64];  // swizzled [t][64 key] tiles
   __nv_bfloat16 Q[2 * BT * 64];  // swizzled [t][64 key] tiles
   __nv_bfloat16 QKM[BT * 64];    // swizzled [t][j] tile
   __nv_bfloat16 dO[BT * (16 * RG + 8)];
@@ -493,12 +493,12 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
       const int lb = si.nblk - 1 - it;
       const int tok0 = si.tok0 + lb * BT, len = min(BT, si.len - lb * BT);
       const size_t bh = (size_t)(si.blk0 + lb) * H + h;
-      const uint32_t bytes = 2 * BT * LDK * 2 + 3 * BT * 64 * 2 + 3 * BT * 4;
+      const uint32_t bytes = 7 * BT * 64 * 2 + 3 * BT * 4;
       if (l == 0) {
         uint64_t* fb = &sm.full[st];
         mbar_arrive_expect_tx(fb, bytes);
-        bulk_g2s(S.W, ws.W + bh * BT * LDK, BT * LDK * 2, fb);
-        bulk_g2s(S.K, ws.Kp + bh * BT * LDK, BT * LDK * 2, fb);
+        bulk_g2s(S.W, ws.W + bh * BT * LDK, 2 * BT * 64 * 2, fb);
+        bulk_g2s(S.K, ws.Kp + bh * BT * LDK, 2 * BT * 64 * 2, fb);
         bulk_g2s(S.Q, ws.Qp + bh * BT * LDK, 2 * BT * 64 * 2, fb);
         bulk_g2s(S.QKM, ws.QKM + bh * BT * LD64, BT * 64 * 2, fb);
         bulk_g2s(S.dec, ws.dec + bh * TC_DEC_ROWS * BT, 3 * BT * 4, fb);
@@ -538,7 +538,7 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
       {
         uint32_t bK[DK / 16][4], bM[4][4];
 #pragma unroll
-        for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_x2n(bK[kc], S.K, LDK, 16 * w, 16 * kc);
+        for (int kc = 0; kc < DK / 16; ++kc) ldb_nk_sw(bK[kc], smem_u32(S.K), 8192, 16 * w, 16 * kc);
 #pragma unroll
         for (int kc = 0; kc < 4; ++kc) ldb_kn_sw(bM[kc], smem_u32(S.QKM), 0, 16 * kc, 16 * w);
 #pragma unroll
@@ -594,8 +594,8 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
       for (int kc = 0; kc < 4; ++kc) {
         ldb_kn_sw(&bQ[kc][0], smem_u32(S.Q), 8192, 16 * kc, 32 * w);
         ldb_kn_sw(&bQ[kc][4], smem_u32(S.Q), 8192, 16 * kc, 32 * w + 16);
-        ldb_kn_x2n(&bW[kc][0], S.W, LDK, 16 * kc, 32 * w);
-        ldb_kn_x2n(&bW[kc][4], S.W, LDK, 16 * kc, 32 * w + 16);
+        ldb_kn_sw(&bW[kc][0], smem_u32(S.W), 8192, 16 * kc, 32 * w);
+        ldb_kn_sw(&bW[kc][4], smem_u32(S.W), 8192, 16 * kc, 32 * w + 16);
       }
       named_bar(1, 128);
       // dH^T <- Gamma_C dH^T + dO^T Q~ - dV^new^T W on key columns [32w, 32w + 32)

@@ -157,7 +157,7 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 struct GradMaps {
   CUtensorMap q, k, v, dout;                 // [B][T][H][d] views
-  CUtensorMap hb, dh, vn, dvn, t, kkm;       // workspace views
+  CUtensorMap hb, dh, vn, dvn, t;            // workspace views
 };
 
 template <int DV>
@@ -239,10 +239,10 @@ __global__ void __launch_bounds__(NTHR, 1)
     mbar_arrive_expect_tx(bar, 8 * KB);
     tma_load_3d(sb + dst, map, 0, 0, it, bar);
   };
-  // Q K^T * Mask: Pre writes it as a swizzled tile, copied as it is
-  auto issue_qkm = [&](int it) {
-    mbar_arrive_expect_tx(barQM, 8 * KB);
-    bulk_g2s(sb + SL::QKM, ws.QKM + (size_t)it * BT * TC_LD64, 8 * KB, barQM);
+  // Q K^T * Mask and K K^T * Mask: Pre writes them as swizzled tiles, copied as they are
+  auto issue_msk = [&](int it, uint32_t dst, const __nv_bfloat16* src, uint64_t* bar) {
+    mbar_arrive_expect_tx(bar, 8 * KB);
+    bulk_g2s(sb + dst, src + (size_t)it * BT * TC_LD64, 8 * KB, bar);
   };
   auto issue_dec = [&](int it, int buf) {
     mbar_arrive_expect_tx(barD + buf, KB);
@@ -318,8 +318,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     issue_qk(it, bi, SL::QQ, &tm.q, barQ);
     issue_qk(it, bi, SL::KK, &tm.k, barK);
     issue_tile(it, SL::TT, &tm.t, barT);
-    issue_qkm(it);
-    issue_tile(it, SL::KKM, &tm.kkm, barKM);
+    issue_msk(it, SL::QKM, ws.QKM, barQM);
+    issue_msk(it, SL::KKM, ws.KKM, barKM);
     issue_dec(it, 0);
   }
   while (it < total) {
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     __syncthreads();
     if (ctl) {
       tc_fence_after();
-      if (more) issue_qkm(nit);  // Q K^T * Mask is read only above
+      if (more) issue_msk(nit, SL::QKM, ws.QKM, barQM);  // Q K^T * Mask is read only above
       // HK^T [s][t] = K . HW^T (rows 64-127)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     __syncthreads();
     if (ctl) {
       tc_fence_after();
-      if (more) issue_tile(nit, SL::KKM, &tm.kkm, barKM);  // K K^T * Mask is free
+      if (more) issue_msk(nit, SL::KKM, ws.KKM, barKM);  // K K^T * Mask is free
       // (BE + BE^T) K, transposed, onto (P^T Q)^T
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -745,8 +745,7 @@ cudaError_t launch_grad(const SeqMap& m, const void* q, const void* k, const voi
       (e = make_ws_map(&tm.dh, ws.dHT, 128, DV, 128, nbh, 128)) ||
       (e = make_ws_map(&tm.vn, ws.VnT, BT, DV, BT, nbh, 128)) ||
       (e = make_ws_map(&tm.dvn, ws.dVnT, BT, DV, BT, nbh, 128)) ||
-      (e = make_ws_map(&tm.t, ws.T, BT, BT, BT, nbh, BT)) ||
-      (e = make_ws_map(&tm.kkm, ws.KKM, BT, BT, TC_LD64, nbh, BT)))
+      (e = make_ws_map(&tm.t, ws.T, BT, BT, BT, nbh, BT)))
     return e;
   const int grid = (int)(items < sms ? items : sms);  // persistent: one CTA per SM
   prof_mark(st, "tc_grad");

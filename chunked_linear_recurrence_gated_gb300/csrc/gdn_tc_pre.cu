@@ -8,10 +8,12 @@
 //   ST  : V^new = U - W H_b ; H_{b+1} = Gamma_C H_b + K^T diag(e^{gamma_C - gamma}) V^new
 //   Out : O = diag(Gamma) Q H_b + QKM V^new
 // Pre also writes decay-scaled copies of the block's rows,
-// K~ = diag(e^{gamma_C - gamma}) K (padded rows) and Q~ = diag(e^{gamma}) Q
-// (128-byte-swizzled tiles, as QKM), and the per-row vectors (Gamma_r,
-// e^{gamma_C - gamma_r}, gamma_r, beta_r), so that the sequential chains fetch
-// every operand with one bulk copy and scale nothing but the state.
+// K~ = diag(e^{gamma_C - gamma}) K and Q~ = diag(e^{gamma}) Q, and the per-row
+// vectors (Gamma_r, e^{gamma_C - gamma_r}, gamma_r, beta_r), so that the
+// sequential chains fetch every operand with one bulk copy and scale nothing
+// but the state. W, K~, Q~, QKM and K K^T * Mask leave in the 128-byte-swizzled
+// layout of a shared-memory tile (sw128), so a bulk copy lands them ready for
+// swizzle-aware fragment loads and tensor-core descriptors.
 //
 // K K^T and Q K^T (64 x 64, reduced over the 128 keys) are warp-level MMAs
 // and the inverse is fp32 with TF32 MMAs for its off-diagonal blocks. W and U
@@ -280,33 +282,28 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
     dec[3 * BT + tid] = s_b[tid];
   }
   __syncthreads();
-  // decay-scaled copies for the chains (one bulk copy each per block):
-  // K~ = diag(e^{gamma_C - gamma}) K with padded rows (the pad columns written
-  // as zeros so every sector is written in full) and Q~ = diag(e^{gamma}) Q
-  // in the swizzled layout of the shared-memory tile (the forward chain's
-  // tensor-core operand)
+  // decay-scaled copies for the chains (one bulk copy each per block),
+  // K~ = diag(e^{gamma_C - gamma}) K and Q~ = diag(e^{gamma}) Q, in the
+  // swizzled layout of the shared-memory tiles
   {
-    uint4* gK = reinterpret_cast<uint4*>(ws.Kp + bh * BT * LDK);
+    unsigned char* gK = reinterpret_cast<unsigned char*>(ws.Kp + bh * BT * LDK);
     unsigned char* gQ = reinterpret_cast<unsigned char*>(ws.Qp + bh * BT * LDK);
-    for (int idx = tid; idx < BT * (LDK / 8); idx += NT) {
-      const int r = idx / (LDK / 8), c = (idx % (LDK / 8)) * 8;
-      uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-      if (c < DK) {
-        const uint32_t off = sw128(r, c, TB);
-        a = *reinterpret_cast<const uint4*>(sb + L::K + off);
-        b = *reinterpret_cast<const uint4*>(sb + L::Q + off);
-        const float sk = s_dte[r], sq = s_G[r];
-        uint32_t* pa = &a.x;
-        uint32_t* pb = &b.x;
+    for (int idx = tid; idx < BT * (DK / 8); idx += NT) {
+      const int r = idx / (DK / 8), c = (idx % (DK / 8)) * 8;
+      const uint32_t off = sw128(r, c, TB);
+      uint4 a = *reinterpret_cast<const uint4*>(sb + L::K + off);
+      uint4 b = *reinterpret_cast<const uint4*>(sb + L::Q + off);
+      const float sk = s_dte[r], sq = s_G[r];
+      uint32_t* pa = &a.x;
+      uint32_t* pb = &b.x;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 x = unpack_bf16(pa[e]), y = unpack_bf16(pb[e]);
-          pa[e] = pack_bf16(sk * x.x, sk * x.y);
-          pb[e] = pack_bf16(sq * y.x, sq * y.y);
-        }
-        *reinterpret_cast<uint4*>(gQ + off) = b;
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = unpack_bf16(pa[e]), y = unpack_bf16(pb[e]);
+        pa[e] = pack_bf16(sk * x.x, sk * x.y);
+        pb[e] = pack_bf16(sq * y.x, sq * y.y);
       }
-      gK[idx] = a;
+      *reinterpret_cast<uint4*>(gK + off) = a;
+      *reinterpret_cast<uint4*>(gQ + off) = b;
     }
   }
 
@@ -349,7 +346,8 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
         sA[r * 68 + c] = br * km0;
         sA[r * 68 + c + 1] = br * km1;
         if (ws.KKM)
-          *reinterpret_cast<uint32_t*>(ws.KKM + bh * BT * LD64 + r * LD64 + c) = pack_bf16(km0, km1);
+          *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(ws.KKM + bh * BT * LD64) +
+                                       sw128(r, c, 0)) = pack_bf16(km0, km1);
         *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(qkm) + sw128(r, c, 0)) =
             pack_bf16(qk[j][2 * hf] * d0, qk[j][2 * hf + 1] * d1);
       }
@@ -389,10 +387,10 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
   ok = __all_sync(0xffffffffu, mbar_wait(mbar, 0, abort)) && ok;  // warp-uniform for tcgen05.ld
   tc_fence_after();
   // read back: lane = key k (W^T) or value v (U^T), 32 tokens per warp; staged as
-  // W [t][k] (padded rows) in A's space and U tile-major at the start
+  // W [t][k] (swizzled 64-key tiles) in A's space and U tile-major at the start
   if (ok) {
     const uint32_t lane_base = tmem + ((uint32_t)(32 * lq) << 16);
-    __nv_bfloat16* Wst = reinterpret_cast<__nv_bfloat16*>(sb + L::A);
+    unsigned char* Wst = sb + L::A;
     __nv_bfloat16* Ust = reinterpret_cast<__nv_bfloat16*>(sb + L::UST);
 #pragma unroll
     for (int part = 0; part <= DV / 128; ++part) {
@@ -402,7 +400,8 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
       if (part == 0) {
         const int kk = 32 * lq + l;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) Wst[(32 * ch + i) * LDK + kk] = __float2bfloat16_rn(vv[i]);
+        for (int i = 0; i < 32; ++i)
+          *reinterpret_cast<__nv_bfloat16*>(Wst + sw128(32 * ch + i, kk, TB)) = __float2bfloat16_rn(vv[i]);
       } else {
         const int vv_ = 128 * (part - 1) + 32 * lq + l;
         __nv_bfloat16* tile = Ust + (size_t)(vv_ >> 4) * BT * LDU;
@@ -411,27 +410,18 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
           tile[u_tile_off(32 * ch + i, vv_ & 15)] = __float2bfloat16_rn(vv[i]);
       }
     }
-    // zero pad columns of the staged W tile
-    for (int r = tid; r < BT; r += NT)
-      *reinterpret_cast<uint4*>(Wst + r * LDK + DK) = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   if (tid == 0) {
     if (ok) {
-      bulk_s2g(ws.W + bh * BT * LDK, sb + L::A, BT * LDK * 2);
+      bulk_s2g(ws.W + bh * BT * LDK, sb + L::A, BT * DK * 2);
       bulk_s2g(ws.U + bh * (DV / 16) * BT * LDU, sb + L::UST, (DV / 16) * BT * LDU * 2);
       bulk_commit();
     } else {
       ws.status[0] = DEV_TIMEOUT;
     }
-  }
-  // zero the pad columns of K K^T * Mask
-  if (ws.KKM) {
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    for (int r = tid; r < BT; r += NT)
-      *reinterpret_cast<uint4*>(ws.KKM + bh * BT * LD64 + r * LD64 + BT) = z;
   }
   if (tid == 0) bulk_wait_read();  // the staged tiles stay valid until read
   __syncthreads();
