@@ -36,7 +36,7 @@ Entry g_cache[kMaxDevices] = {};
 typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
 // The current context of the calling thread (nullptr if none is current yet
-// or the driver entry point is unavailable).
+// or the CUDA driver-API entry point is unavailable).
 void* current_context() {
   static CtxGetCurrentFn fn = nullptr;
   static bool looked_up = false;
