@@ -50,13 +50,13 @@ struct PreLayout {
   static constexpr uint32_t K = 0;                 // K (swizzled)
   static constexpr uint32_t V = 16384;             // V (swizzled), DV / 64 tiles
   static constexpr uint32_t Q = V + DV * 128;      // Q (swizzled)
-  static constexpr uint32_t A = Q;                 // fp32 A [64][68]; then TW, TU; then W [64][LDK]
+  static constexpr uint32_t A = Q;                 // fp32 A (fix layout); then TW, TU; then W
   static constexpr uint32_t TW = A;                // T diag(beta Gamma) [64][64] (swizzled)
   static constexpr uint32_t TU = A + 8192;         // T diag(beta) [64][64] (swizzled)
-  static constexpr uint32_t TF = A + 17408;        // fp32 T [64][68]
-  static constexpr uint32_t S = TF + 17408;        // fp32 [16][52] block-row product
+  static constexpr uint32_t TF = A + 18432;        // fp32 T (fix layout)
+  static constexpr uint32_t S = TF + 18432;        // fp32 [16] rows, block-row product (fix layout)
   static constexpr uint32_t UST = 0;               // U, tile-major [DV/16][64][LDU] (u_tile_off)
-  static constexpr uint32_t VEC = S + 4096;
+  static constexpr uint32_t VEC = S + 4608;
   static constexpr uint32_t BYTES = VEC + 4 * 256 + 64;
   static constexpr uint32_t NCOL = DV == 128 ? 128 : 256;  // TMEM: W^T [0, 64), U^T [64, 64 + DV/2)
   static constexpr int CTAS = DV == 128 ? 3 : 2;          // per SM
@@ -105,7 +105,16 @@ __device__ __forceinline__ void block_cumsum64(float* sg) {
   }
 }
 
-// T = (I + A)^-1 for strictly-lower 64 x 64 A (fp32, ld 68), NT threads.
+// fp32 tiles of the inverse: element (r, c) at word fix(r, c), rows of 72
+// words with column bit 2 flipped on rows whose bit 2 is set, so the TF32
+// fragment loads of either operand role, the float2 fragment stores and the
+// diagonal blocks' row stores hit 32 distinct banks.
+__device__ __forceinline__ int fix(int r, int c) { return r * 72 + (c ^ (((r >> 2) & 1) << 2)); }
+__device__ __forceinline__ void st2(float* base, int r, int c, float x, float y) {  // c even
+  *reinterpret_cast<float2*>(base + fix(r, c)) = make_float2(x, y);
+}
+
+// T = (I + A)^-1 for strictly-lower 64 x 64 A (fp32, fix layout), NT threads.
 // The four diagonal 16 x 16 blocks by fp32 forward substitution (one warp
 // each); then, block row by block row (i = 1..3), warps 0..2i-1 (one n8
 // column tile each) form
@@ -115,7 +124,7 @@ __device__ __forceinline__ void block_cumsum64(float* sg) {
 template <int NT>
 __device__ void invert_unit_lower64(const float* A, float* Tf, float* S) {
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, g = l >> 2, t = l & 3;
-  for (int idx = tid; idx < BT * 68; idx += NT) Tf[idx] = 0.f;
+  for (int idx = tid; idx < BT * 72; idx += NT) Tf[idx] = 0.f;
   __syncthreads();
   if (w < 4 && l < 16) {
     const int c = 16 * w + l;
@@ -123,11 +132,10 @@ __device__ void invert_unit_lower64(const float* A, float* Tf, float* S) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       float v = (r == l) ? 1.f : 0.f;
-      const float* Ar = A + (16 * w + r) * 68 + 16 * w;
 #pragma unroll
-      for (int j = 0; j < r; ++j) v -= Ar[j] * x[j];
+      for (int j = 0; j < r; ++j) v -= A[fix(16 * w + r, 16 * w + j)] * x[j];
       x[r] = v;
-      Tf[(16 * w + r) * 68 + c] = v;
+      Tf[fix(16 * w + r, c)] = v;
     }
   }
   __syncthreads();
@@ -139,40 +147,36 @@ __device__ void invert_unit_lower64(const float* A, float* Tf, float* S) {
     const int R = 16 * i;
     if (w < 2 * i) {
       const int nt = w;
-      // S (16 x 8, column tile nt) = A[R:R+16, 0:16i] * Tf[0:16i, 8nt:8nt+8]; fp32, ld 52
+      // S (16 x 8, column tile nt) = A[R:R+16, 0:16i] * Tf[0:16i, 8nt:8nt+8]; fp32
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kt = 0; kt < 2 * i; ++kt) {
         uint32_t a[4];
-        a[0] = to_tf32(A[(R + g) * 68 + 8 * kt + t]);
-        a[1] = to_tf32(A[(R + g + 8) * 68 + 8 * kt + t]);
-        a[2] = to_tf32(A[(R + g) * 68 + 8 * kt + t + 4]);
-        a[3] = to_tf32(A[(R + g + 8) * 68 + 8 * kt + t + 4]);
-        const uint32_t b0 = to_tf32(Tf[(8 * kt + t) * 68 + 8 * nt + g]);
-        const uint32_t b1 = to_tf32(Tf[(8 * kt + t + 4) * 68 + 8 * nt + g]);
+        a[0] = to_tf32(A[fix(R + g, 8 * kt + t)]);
+        a[1] = to_tf32(A[fix(R + g + 8, 8 * kt + t)]);
+        a[2] = to_tf32(A[fix(R + g, 8 * kt + t + 4)]);
+        a[3] = to_tf32(A[fix(R + g + 8, 8 * kt + t + 4)]);
+        const uint32_t b0 = to_tf32(Tf[fix(8 * kt + t, 8 * nt + g)]);
+        const uint32_t b1 = to_tf32(Tf[fix(8 * kt + t + 4, 8 * nt + g)]);
         mma_tf32(acc, a, b0, b1);
       }
-      S[g * 52 + 8 * nt + 2 * t] = acc[0];
-      S[g * 52 + 8 * nt + 2 * t + 1] = acc[1];
-      S[(g + 8) * 52 + 8 * nt + 2 * t] = acc[2];
-      S[(g + 8) * 52 + 8 * nt + 2 * t + 1] = acc[3];
+      st2(S, g, 8 * nt + 2 * t, acc[0], acc[1]);
+      st2(S, g + 8, 8 * nt + 2 * t, acc[2], acc[3]);
       __syncwarp();
       // T[R:R+16, 8nt:8nt+8] = -T_ii S
       float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kt = 0; kt < 2; ++kt) {
         uint32_t a[4];
-        a[0] = to_tf32(Tf[(R + g) * 68 + R + 8 * kt + t]);
-        a[1] = to_tf32(Tf[(R + g + 8) * 68 + R + 8 * kt + t]);
-        a[2] = to_tf32(Tf[(R + g) * 68 + R + 8 * kt + t + 4]);
-        a[3] = to_tf32(Tf[(R + g + 8) * 68 + R + 8 * kt + t + 4]);
-        const uint32_t b0 = to_tf32(S[(8 * kt + t) * 52 + 8 * nt + g]);
-        const uint32_t b1 = to_tf32(S[(8 * kt + t + 4) * 52 + 8 * nt + g]);
+        a[0] = to_tf32(Tf[fix(R + g, R + 8 * kt + t)]);
+        a[1] = to_tf32(Tf[fix(R + g + 8, R + 8 * kt + t)]);
+        a[2] = to_tf32(Tf[fix(R + g, R + 8 * kt + t + 4)]);
+        a[3] = to_tf32(Tf[fix(R + g + 8, R + 8 * kt + t + 4)]);
+        const uint32_t b0 = to_tf32(S[fix(8 * kt + t, 8 * nt + g)]);
+        const uint32_t b1 = to_tf32(S[fix(8 * kt + t + 4, 8 * nt + g)]);
         mma_tf32(acc2, a, b0, b1);
       }
-      Tf[(R + g) * 68 + 8 * nt + 2 * t] = -acc2[0];
-      Tf[(R + g) * 68 + 8 * nt + 2 * t + 1] = -acc2[1];
-      Tf[(R + g + 8) * 68 + 8 * nt + 2 * t] = -acc2[2];
-      Tf[(R + g + 8) * 68 + 8 * nt + 2 * t + 1] = -acc2[3];
+      st2(Tf, R + g, 8 * nt + 2 * t, -acc2[0], -acc2[1]);
+      st2(Tf, R + g + 8, 8 * nt + 2 * t, -acc2[2], -acc2[3]);
     }
     __syncthreads();
   }
@@ -343,8 +347,7 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
         const float br = s_b[r];
         const float km0 = (c < r) ? kk[j][2 * hf] * d0 : 0.f;
         const float km1 = (c + 1 < r) ? kk[j][2 * hf + 1] * d1 : 0.f;
-        sA[r * 68 + c] = br * km0;
-        sA[r * 68 + c + 1] = br * km1;
+        st2(sA, r, c, br * km0, br * km1);
         if (ws.KKM)
           *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(ws.KKM + bh * BT * LD64) +
                                        sw128(r, c, 0)) = pack_bf16(km0, km1);
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
   // Tw = T diag(beta Gamma), Tu = T diag(beta) as swizzled [t][j] tiles; T itself for the backward
   for (int idx = 2 * tid; idx < BT * BT; idx += 2 * NT) {  // column pairs
     const int r = idx >> 6, c = idx & 63;
-    const float2 t = *reinterpret_cast<const float2*>(&sTf[r * 68 + c]);
+    const float2 t = *reinterpret_cast<const float2*>(&sTf[fix(r, c)]);
     const float2 bc = *reinterpret_cast<const float2*>(&s_b[c]);
     const float2 Gc = *reinterpret_cast<const float2*>(&s_G[c]);
     *reinterpret_cast<uint32_t*>(sb + L::TW + sw128(r, c, 0)) =
@@ -405,9 +408,12 @@ __global__ void __launch_bounds__(256, PreLayout<DV>::CTAS)
       } else {
         const int vv_ = 128 * (part - 1) + 32 * lq + l;
         __nv_bfloat16* tile = Ust + (size_t)(vv_ >> 4) * BT * LDU;
+        // lanes 16-31 fill the next 16-value tile, whose rows sit on the same
+        // banks: they take the tokens in swapped pairs, so each store is one wavefront
+        const bool hi = l >= 16;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          tile[u_tile_off(32 * ch + i, vv_ & 15)] = __float2bfloat16_rn(vv[i]);
+          tile[u_tile_off(32 * ch + (hi ? (i ^ 1) : i), vv_ & 15)] = __float2bfloat16_rn(hi ? vv[i ^ 1] : vv[i]);
       }
     }
   }
