@@ -29,7 +29,9 @@ void prof_mark(cudaStream_t st, const char* next) {
 // numbers the 64-token blocks of every sequence (each sequence's grid starts
 // at its first token) and records the owning sequence of each block. A
 // malformed array sets the status word and leaves every table empty, so no
-// kernel does any work.
+// kernel does any work. order (blk0 + nseq + 1) lists the sequences longest
+// first (ties by index; index order past 4096 sequences): the sequential
+// chains start their CTAs in that order, so the longest chains do not trail.
 __global__ void k_varlen_prep(const int* __restrict__ cu, int nseq, int T, int nblk_cap,
                               int* blk0, int* blk_seq, int* status) {
   __shared__ int bad;
@@ -52,11 +54,25 @@ __global__ void k_varlen_prep(const int* __restrict__ cu, int nseq, int T, int n
   if (bad) {
     for (int gb = threadIdx.x; gb < nblk_cap; gb += blockDim.x) blk_seq[gb] = -1;
     for (int s = threadIdx.x; s <= nseq; s += blockDim.x) blk0[s] = 0;
+    for (int s = threadIdx.x; s < nseq; s += blockDim.x) blk0[nseq + 1 + s] = s;
     return;
   }
   for (int s = threadIdx.x; s < nseq; s += blockDim.x)
     for (int gb = blk0[s]; gb < blk0[s + 1]; ++gb) blk_seq[gb] = s;
   for (int gb = blk0[nseq] + threadIdx.x; gb < nblk_cap; gb += blockDim.x) blk_seq[gb] = -1;
+  int* order = blk0 + nseq + 1;
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    int rank = s;
+    if (nseq <= 4096) {
+      const int n = blk0[s + 1] - blk0[s];
+      rank = 0;
+      for (int o = 0; o < nseq; ++o) {
+        const int no = blk0[o + 1] - blk0[o];
+        rank += (no > n || (no == n && o < s)) ? 1 : 0;
+      }
+    }
+    order[rank] = s;
+  }
 }
 
 cudaError_t varlen_prep(const int* cu, int nseq, int T, int nblk_cap, int* blk0, int* blk_seq,
@@ -157,7 +173,8 @@ size_t simt_layout(const Plan& p, bool bwd, SimtWs* ws, int** blk0, int** blk_se
   Carve c;
   const size_t nbh = (size_t)p.nblk_cap * p.H;
   const size_t o_status = c.take(kAlign);
-  const size_t o_blk0 = p.varlen ? c.take(sizeof(int) * (p.nseq + 1)) : 0;
+  // blk0 [nseq + 1], then the sequences in the order the chains take them [nseq]
+  const size_t o_blk0 = p.varlen ? c.take(sizeof(int) * (2 * (size_t)p.nseq + 1)) : 0;
   const size_t o_blks = p.varlen ? c.take(sizeof(int) * (size_t)p.nblk_cap) : 0;
   const size_t o_gam = c.take(4 * nbh * BT);
   const size_t o_W = c.take(4 * nbh * BT * p.dk);
@@ -236,7 +253,8 @@ size_t tc_layout(const Plan& p, int kind, TcWs* ws, int** blk0, int** blk_seq, c
   const bool bwd = kind != WS_FWD;
   const size_t nbh = (size_t)p.nblk_cap * p.H;
   const size_t o_status = c.take(kAlign);
-  const size_t o_blk0 = p.varlen ? c.take(sizeof(int) * (p.nseq + 1)) : 0;
+  // blk0 [nseq + 1], then the sequences in the order the chains take them [nseq]
+  const size_t o_blk0 = p.varlen ? c.take(sizeof(int) * (2 * (size_t)p.nseq + 1)) : 0;
   const size_t o_blks = p.varlen ? c.take(sizeof(int) * (size_t)p.nblk_cap) : 0;
   if (kind != WS_SAVED) {
     Carve pc;
@@ -308,6 +326,7 @@ SeqMap make_map(const Plan& p, const int* cu, const int* blk0, const int* blk_se
   m.cu = p.varlen ? cu : nullptr;
   m.blk0 = blk0;
   m.blk_seq = blk_seq;
+  m.order = p.varlen ? blk0 + p.nseq + 1 : nullptr;
   m.nseq = p.nseq;
   m.T_fixed = p.varlen ? 0 : p.T;
   m.nblk_fixed = p.varlen ? 0 : (p.T + BT - 1) / BT;

@@ -22,6 +22,7 @@ struct SeqMap {
   const int* cu;       // varlen: device cu_seqlens [nseq + 1]; fixed: nullptr
   const int* blk0;     // varlen: first global block of each sequence [nseq + 1]
   const int* blk_seq;  // varlen: owning sequence of each global block (-1 = none)
+  const int* order;    // varlen: sequences longest first (the chains' CTA order); fixed: nullptr
   int nseq;
   int T_fixed;         // fixed: tokens per sequence
   int nblk_fixed;      // fixed: blocks per sequence

@@ -135,7 +135,7 @@ __device__ __forceinline__ void chain_fwd_body(const SeqMap& m, int cta,
   constexpr int LDO = BV + 8;
   const int tile = cta % NVT;
   const int sh = cta / NVT;
-  const int H = m.H, h = sh % H, s = sh / H;
+  const int H = m.H, h = sh % H, s = m.order ? m.order[sh / H] : sh / H;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
   const SeqInfo si = seq_info(m, s);
   const int nb = max(0, min(si.nblk, lb1) - lb0);  // blocks this launch carries
@@ -443,7 +443,7 @@ __device__ __forceinline__ void chain_rev_body(const SeqMap& m, int cta,
   constexpr int LDO = BV + 8;
   const int tile = cta % NVT;
   const int sh = cta / NVT;
-  const int H = m.H, h = sh % H, s = sh / H;
+  const int H = m.H, h = sh % H, s = m.order ? m.order[sh / H] : sh / H;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, gq = l >> 2, tq = l & 3;
   const SeqInfo si = seq_info(m, s);
   RevSmem<RG>& sm = *reinterpret_cast<RevSmem<RG>*>(smraw);
